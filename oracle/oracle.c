@@ -1,0 +1,329 @@
+/*
+ * oracle.c -- plain, slow CPU reference for the dense tensor-core GEMM
+ *
+ *     D = alpha * A * B + beta * C
+ *
+ * with BF16 or FP8 E4M3 operands, computed exactly (up to FP64 rounding).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * under tensor_core_dense_gb300/) may include, link or call this file; only
+ * tests/, the smoke check in __graft_entry__.py and bench.py's CPU-baseline
+ * leg use it.  It shares no code, header, table or constant with the CUDA
+ * path.
+ *
+ * What it computes, and where that comes from:
+ *
+ *  - The operation is the multiply-accumulate D = A*B + C with A an M x K
+ *    matrix, B a K x N matrix and C, D M x N ("Tensor Cores: Matrix
+ *    Instructions, Swizzling and FP8, Measured", Step 1; "Tensor Cores",
+ *    "What a Tensor Core does"), extended by the alpha/beta scalars and the
+ *    FP8 scale factors of the FP8 recipe ("Tensor cores and low precision",
+ *    paragraph on FP8 scaling: scale before the cast, remove the scale after
+ *    the multiply).
+ *  - B is held N x K with K contiguous, the "TN" layout of the 4,096^3 test
+ *    ("Tensor Cores: Matrix Instructions, ...", Step 2): element (k, j) of B
+ *    sits at B[j * ldb + k].  A is M x K row-major: A[i * lda + k].
+ *  - BF16 is 1 sign / 8 exponent / 7 mantissa bits, the top half of an FP32
+ *    word ("Tensor Cores", "Precision: FP16, BF16, TF32, FP8").
+ *  - E4M3 is 1 / 4 / 3 bits, no infinities, maximum normal 448 ("Tensor
+ *    cores and low precision", paragraph on the two 8-bit encodings).  448 =
+ *    1.75 * 2^8 is the largest finite value with exponent field 15 and
+ *    mantissa 110, so the exponent bias is 7 and only mantissa 111 at
+ *    exponent 15 is NaN.
+ *
+ * Accumulation is in FP64.  BF16 x BF16 products are exact in FP64.  For
+ * E4M3 the raw code products q_a * q_b (at most 8 significant bits, exponents
+ * 2^-18 .. 2^17) are summed per 128-wide K block, which is exact, and only
+ * then multiplied by the block's FP64 scale product s_a * s_b (exact, 24+24
+ * bits).  The sum of |a_ik * b_kj| is returned beside each value as the
+ * error bound the tolerances are stated against.
+ *
+ * The scale layouts for the 128-block mode (the pages name block scaling but
+ * give no storage order; this is the library's choice, stated here and in
+ * its header):
+ *     a_scale[kb * M + i]          scale of A row i, K block kb   (1 x 128)
+ *     b_scale[nb * KB + kb]        scale of B rows 128nb.., K block kb
+ *                                   (128 x 128), KB = ceil(K / 128)
+ *
+ * Portable C11, no intrinsics; compiled with -ffp-contract=off so x86 and
+ * Arm hosts round identically.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_IN_BF16 0
+#define ORC_IN_E4M3 1
+#define ORC_SCALE_NONE 0   /* BF16: no scales */
+#define ORC_SCALE_TENSOR 1 /* one scale per operand */
+#define ORC_SCALE_BLOCK128 2
+#define ORC_C_BF16 0
+#define ORC_C_F32 1
+
+/* ------------------------------------------------------------------ codecs */
+
+/* BF16 bits -> value: the 16 bits are the high half of an FP32 word. */
+double orc_bf16_decode(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* FP32 -> BF16 with round-to-nearest, ties to even, on the 16 dropped bits.
+ * NaN stays a quiet NaN with its sign; overflow rounds to infinity. */
+uint16_t orc_bf16_encode(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+    return (uint16_t)(((u >> 16) & 0x8000u) | 0x7FC0u);
+  uint32_t dropped = u & 0xFFFFu;
+  uint32_t kept = u >> 16;
+  if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u))) kept += 1u;
+  return (uint16_t)kept;
+}
+
+/* E4M3 bits -> value.  S.EEEE.MMM, bias 7; exponent field 0 is subnormal
+ * (M/8 * 2^-6); S.1111.111 is NaN; there is no infinity. */
+double orc_e4m3_decode(uint8_t b) {
+  int s = (b >> 7) & 1;
+  int e = (b >> 3) & 15;
+  int m = b & 7;
+  if (e == 15 && m == 7) return NAN;
+  double mag = (e == 0) ? ldexp((double)m, -9)           /* (m/8) * 2^-6 */
+                        : ldexp((double)(8 + m), e - 10); /* (1+m/8) * 2^(e-7) */
+  return s ? -mag : mag;
+}
+
+/* FP32 -> E4M3, round to nearest even on the E4M3 grid, saturating: any
+ * finite or infinite magnitude that rounds above 448 becomes +-448.  NaN ->
+ * 0x7F (sign kept).  The rounding is done on integers (the FP32 significand
+ * and exponent), with no floating-point arithmetic. */
+uint8_t orc_e4m3_encode(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+  uint32_t a = u & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return (uint8_t)(sign | 0x7Fu);
+  if (a == 0x7F800000u) return (uint8_t)(sign | 0x7Eu);
+  int ef = (int)(a >> 23);
+  if (ef == 0) return sign; /* FP32 zero or subnormal (< 2^-126): rounds to 0 */
+  uint64_t sig = (uint64_t)((a & 0x7FFFFFu) | 0x800000u); /* value = sig * 2^(E-23) */
+  int E = ef - 127;
+  /* E4M3 quantum at this magnitude: 2^(E-3) for normals (E >= -6), else the
+   * subnormal step 2^-9. */
+  int q = (E >= -6) ? E - 3 : -9;
+  int shift = 23 + q - E; /* bits of sig below the quantum, >= 20 */
+  uint64_t r;             /* magnitude rounded, in units of 2^q */
+  if (shift >= 40) {
+    r = 0;
+  } else {
+    uint64_t keep = sig >> shift;
+    uint64_t rem = sig & ((1ull << shift) - 1ull);
+    uint64_t half = 1ull << (shift - 1);
+    r = keep + ((rem > half || (rem == half && (keep & 1ull))) ? 1u : 0u);
+  }
+  /* Re-express r * 2^q as exponent field / mantissa.  r * 2^q with q = -9 and
+   * r < 8 is a subnormal; otherwise normalise so the significand is 8..15. */
+  if (q == -9 && r < 8) return (uint8_t)(sign | (uint8_t)r);
+  int qq = q;
+  while (r >= 16) { /* rounding carried into the next binade */
+    r >>= 1;        /* r was even (a multiple of 16), exact */
+    qq += 1;
+  }
+  /* value = r * 2^qq with 8 <= r <= 15, i.e. (1 + (r-8)/8) * 2^(qq+3) */
+  int e_unb = qq + 3;
+  int efield = e_unb + 7;
+  if (efield > 15 || (efield == 15 && (r - 8) >= 7)) return (uint8_t)(sign | 0x7Eu);
+  return (uint8_t)(sign | (uint8_t)(efield << 3) | (uint8_t)(r - 8));
+}
+
+void orc_bf16_decode_array(const uint16_t* in, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_decode(in[i]);
+}
+void orc_bf16_encode_array(const float* in, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_encode(in[i]);
+}
+void orc_e4m3_decode_array(const uint8_t* in, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(in[i]);
+}
+void orc_e4m3_encode_array(const float* in, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(in[i]);
+}
+
+/* The BF16 output the library is expected to store for an FP64 value v:
+ * v rounded to FP32, then to BF16 with ties to even. */
+void orc_cast_bf16_array(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_encode((float)v[i]);
+}
+
+/* -------------------------------------------------------------------- GEMM */
+
+typedef struct {
+  int64_t M, N, K;
+  int32_t in_type;    /* ORC_IN_BF16 / ORC_IN_E4M3 */
+  int32_t scale_mode; /* ORC_SCALE_* */
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  const float* a_scale;
+  const float* b_scale;
+  const void* C; /* may be NULL when beta == 0 */
+  int64_t ldc;
+  int32_t c_type; /* ORC_C_BF16 / ORC_C_F32 */
+  int32_t pad_;
+  double alpha, beta;
+} orc_gemm_args;
+
+static double dec_in(const orc_gemm_args* g, const void* base, int64_t idx) {
+  if (g->in_type == ORC_IN_BF16) return orc_bf16_decode(((const uint16_t*)base)[idx]);
+  return orc_e4m3_decode(((const uint8_t*)base)[idx]);
+}
+
+static double dec_c(const orc_gemm_args* g, int64_t i, int64_t j) {
+  int64_t idx = i * g->ldc + j;
+  if (g->c_type == ORC_C_BF16) return orc_bf16_decode(((const uint16_t*)g->C)[idx]);
+  return (double)((const float*)g->C)[idx];
+}
+
+/* One output element.  Sums run over k in ascending order. */
+static void gemm_one(const orc_gemm_args* g, const double* arow, const double* brow, int64_t i,
+                     int64_t j, double* v_out, double* bound_out) {
+  const int64_t K = g->K;
+  double acc = 0.0, bound = 0.0;
+  if (g->scale_mode == ORC_SCALE_BLOCK128) {
+    const int64_t KB = (K + 127) / 128;
+    const int64_t nb = j / 128;
+    for (int64_t kb = 0; kb < KB; ++kb) {
+      double part = 0.0, apart = 0.0;
+      int64_t k1 = (kb + 1) * 128 < K ? (kb + 1) * 128 : K;
+      for (int64_t k = kb * 128; k < k1; ++k) {
+        double p = arow[k] * brow[k];
+        part += p;
+        apart += fabs(p);
+      }
+      double s = (double)g->a_scale[kb * g->M + i] * (double)g->b_scale[nb * KB + kb];
+      acc += part * s;
+      bound += apart * fabs(s);
+    }
+  } else {
+    for (int64_t k = 0; k < K; ++k) {
+      double p = arow[k] * brow[k];
+      acc += p;
+      bound += fabs(p);
+    }
+    if (g->scale_mode == ORC_SCALE_TENSOR) {
+      double s = (double)g->a_scale[0] * (double)g->b_scale[0];
+      acc *= s;
+      bound *= fabs(s);
+    }
+  }
+  double v = g->alpha * acc;
+  if (g->beta != 0.0) v += g->beta * dec_c(g, i, j);
+  *v_out = v;
+  *bound_out = fabs(g->alpha) * bound;
+}
+
+/* One rectangular block of outputs: rows i0..i0+mi-1, columns j0..j0+nj-1,
+ * written row-major into v[mi*nj] and bound[mi*nj]. */
+static int gemm_tile(const orc_gemm_args* g, int64_t i0, int64_t j0, int64_t mi, int64_t nj,
+                     double* v, double* bound) {
+  const int64_t K = g->K;
+  double* arows = (double*)malloc((size_t)(mi * (K > 0 ? K : 1)) * sizeof(double));
+  double* brows = (double*)malloc((size_t)(nj * (K > 0 ? K : 1)) * sizeof(double));
+  if (!arows || !brows) {
+    free(arows);
+    free(brows);
+    return -1;
+  }
+  for (int64_t r = 0; r < mi; ++r)
+    for (int64_t k = 0; k < K; ++k) arows[r * K + k] = dec_in(g, g->A, (i0 + r) * g->lda + k);
+  for (int64_t c = 0; c < nj; ++c)
+    for (int64_t k = 0; k < K; ++k) brows[c * K + k] = dec_in(g, g->B, (j0 + c) * g->ldb + k);
+  for (int64_t r = 0; r < mi; ++r)
+    for (int64_t c = 0; c < nj; ++c)
+      gemm_one(g, arows + r * K, brows + c * K, i0 + r, j0 + c, &v[r * nj + c], &bound[r * nj + c]);
+  free(arows);
+  free(brows);
+  return 0;
+}
+
+typedef struct {
+  const orc_gemm_args* g;
+  const int64_t* tiles; /* [n][4]: i0, j0, mi, nj */
+  const int64_t* offs;  /* output offset of each tile */
+  int64_t ntiles;
+  int64_t next; /* next tile index to take (guarded by mu) */
+  pthread_mutex_t mu;
+  double* v;
+  double* bound;
+  int err;
+} work_t;
+
+static void* worker(void* p) {
+  work_t* w = (work_t*)p;
+  for (;;) {
+    pthread_mutex_lock(&w->mu);
+    int64_t t = w->next++;
+    pthread_mutex_unlock(&w->mu);
+    if (t >= w->ntiles) break;
+    const int64_t* d = w->tiles + 4 * t;
+    if (gemm_tile(w->g, d[0], d[1], d[2], d[3], w->v + w->offs[t], w->bound + w->offs[t]) != 0) {
+      pthread_mutex_lock(&w->mu);
+      w->err = -1;
+      pthread_mutex_unlock(&w->mu);
+    }
+  }
+  return NULL;
+}
+
+/* Compute a list of output tiles.  tiles[4*t .. 4*t+3] = (i0, j0, mi, nj);
+ * tile t's values land row-major at v + sum_{u<t} mi_u * nj_u (same for
+ * bound).  Tiles are taken by `nthreads` worker threads; each tile is
+ * computed by one thread, so the result does not depend on nthreads.
+ * Returns 0, or -1 on a bad argument or allocation failure. */
+int orc_gemm_tiles(const orc_gemm_args* g, int64_t ntiles, const int64_t* tiles, double* v,
+                   double* bound, int nthreads) {
+  if (!g || ntiles < 0 || (ntiles > 0 && (!tiles || !v || !bound))) return -1;
+  if (g->M < 0 || g->N < 0 || g->K < 0) return -1;
+  if (g->K > 0 && (!g->A || !g->B)) return -1;
+  if (g->beta != 0.0 && !g->C) return -1;
+  if (g->scale_mode != ORC_SCALE_NONE && (!g->a_scale || !g->b_scale)) return -1;
+  int64_t* offs = (int64_t*)malloc((size_t)(ntiles > 0 ? ntiles : 1) * sizeof(int64_t));
+  if (!offs) return -1;
+  int64_t o = 0;
+  for (int64_t t = 0; t < ntiles; ++t) {
+    const int64_t* d = tiles + 4 * t;
+    if (d[0] < 0 || d[1] < 0 || d[2] < 0 || d[3] < 0 || d[0] + d[2] > g->M || d[1] + d[3] > g->N) {
+      free(offs);
+      return -1;
+    }
+    offs[t] = o;
+    o += d[2] * d[3];
+  }
+  work_t w;
+  w.g = g;
+  w.tiles = tiles;
+  w.offs = offs;
+  w.ntiles = ntiles;
+  w.next = 0;
+  w.v = v;
+  w.bound = bound;
+  w.err = 0;
+  pthread_mutex_init(&w.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&th[started], NULL, worker, &w) == 0) ++started;
+  }
+  worker(&w);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  pthread_mutex_destroy(&w.mu);
+  free(offs);
+  return w.err;
+}

@@ -1,0 +1,339 @@
+"""Pins for the CPU oracle (runs without a GPU).
+
+Each test ties the oracle to something other than itself: facts the pages
+print (tests/golden/), library implementations of the same number formats
+(torch's bfloat16 and float8_e4m3fn conversions), closed forms, and exact
+brute force with Python rationals on tiny shapes.
+"""
+
+import math
+import os
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ----------------------------------------------------------------- E4M3 codec
+
+def test_e4m3_facts_from_the_pages():
+    facts = {r[0]: r[1] for r in _golden("e4m3_format.txt")}
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes)
+    finite = vals[np.isfinite(vals)]
+    assert finite.max() == float(facts["e4m3_max_normal"]) == 448.0
+    assert -finite.min() == 448.0
+    assert not np.isinf(vals).any()                     # no infinities
+    assert np.isnan(vals).sum() == 2                     # only S.1111.111
+    assert np.isnan(vals[0x7F]) and np.isnan(vals[0xFF])
+    assert vals[0x7E] == 448.0
+    # 1 + 4 + 3 bits: 2^4 binades of 2^3 mantissas per sign
+    assert int(facts["e4m3_exponent_bits"]) + int(facts["e4m3_mantissa_bits"]) + 1 == 8
+
+
+def test_e4m3_decode_matches_torch_float8_for_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    m = ~np.isnan(ref)
+    assert np.array_equal(ref[m], got[m])
+    assert np.array_equal(np.signbit(ref[m]), np.signbit(got[m]))  # -0 kept
+
+
+def test_e4m3_decode_monotone_and_subnormal_step():
+    v = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    assert (np.diff(v) > 0).all()
+    assert v[1] == 2.0 ** -9 and v[8] == 2.0 ** -6 and v[0x38] == 1.0
+    neg = oracle.e4m3_decode(np.arange(0x80, 0xFF, dtype=np.uint8))
+    assert np.array_equal(neg, -v)
+
+
+def test_e4m3_encode_round_trip_and_saturation():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+    sat = np.array([448.0, 449.0, 464.0, 465.0, 480.0, 1e6, np.inf], dtype=np.float32)
+    assert (oracle.e4m3_encode(sat) == 0x7E).all()
+    assert (oracle.e4m3_encode(-sat) == 0xFE).all()
+    assert oracle.e4m3_encode(np.array([np.nan], dtype=np.float32))[0] in (0x7F, 0xFF)
+
+
+def test_e4m3_encode_midpoints_round_to_even():
+    pos = oracle.e4m3_decode(np.arange(0, 0x7E, dtype=np.uint8))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)  # exact in FP32
+    enc = oracle.e4m3_encode(mids)
+    lo = np.arange(0, 0x7D, dtype=np.uint8)
+    expect = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint8)
+    assert np.array_equal(enc, expect)
+
+
+def test_e4m3_encode_matches_torch_and_the_input_generator():
+    rng = np.random.default_rng(0)
+    # every 2^9-th FP32 pattern of magnitude below 448 plus random values
+    bits = np.arange(0, 0x43E00000, 512, dtype=np.uint32)
+    x = np.concatenate([bits.view(np.float32), -bits.view(np.float32),
+                        rng.normal(0, 50, 200_000).astype(np.float32).clip(-448, 448)])
+    got = oracle.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+    assert np.array_equal(got, synth.to_e4m3(x))
+
+
+# ----------------------------------------------------------------- BF16 codec
+
+def test_bf16_decode_matches_torch_for_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.bf16_decode(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+
+
+def test_bf16_encode_matches_torch_round_trip_and_ties():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([
+        rng.standard_normal(500_000).astype(np.float32),
+        (rng.standard_normal(100_000) * 1e30).astype(np.float32),
+        np.array([3.3895314e38, 3.4028235e38, -3.4028235e38, 1e-40, -0.0, np.inf], np.float32)])
+    got = oracle.bf16_encode(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    assert np.array_equal(got, synth.to_bf16(x))
+    # round trip of every non-NaN pattern
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_decode(bits)
+    keep = ~np.isnan(vals)
+    assert np.array_equal(oracle.bf16_encode(vals[keep].astype(np.float32)), bits[keep])
+    # ties: 1 + 2^-8 sits halfway between 1 and 1 + 2^-7 -> even (1.0)
+    ties = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8], dtype=np.float32)
+    assert list(oracle.bf16_decode(oracle.bf16_encode(ties))) == [1.0, 1 + 2 ** -6]
+
+
+# -------------------------------------------------------------- GEMM, exact
+
+def _exact_gemm(M, N, K, a, b, alpha=1, beta=0, c=None, sa=None, sb=None, block=False):
+    """Brute force with rationals: a[i][k], b[j][k] are Fractions (decoded)."""
+    KB = (K + 127) // 128
+    out = [[Fraction(0)] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = Fraction(0)
+            for k in range(K):
+                p = a[i][k] * b[j][k]
+                if block:
+                    p *= Fraction(float(sa[(k // 128) * M + i])) * Fraction(
+                        float(sb[(j // 128) * KB + k // 128]))
+                elif sa is not None:
+                    p *= Fraction(float(sa[0])) * Fraction(float(sb[0]))
+                s += p
+            v = Fraction(alpha) * s
+            if beta != 0:
+                v += Fraction(beta) * c[i][j]
+            out[i][j] = v
+    return out
+
+
+def _frac_rows(vals, rows, cols, ld):
+    return [[Fraction(float(vals[r * ld + c])) for c in range(cols)] for r in range(rows)]
+
+
+def test_m16n8k16_worked_example_all_128_outputs_exact():
+    facts = {r[0]: r[1:] for r in _golden("mma_m16n8k16_example.txt")}
+    m, n, k = int(facts["m"][0]), int(facts["n"][0]), int(facts["k"][0])
+    assert 2 * m * n * k == int(facts["flops"][0])
+    rng = np.random.default_rng(16)
+    ai = rng.integers(-8, 9, size=(m, k))
+    bi = rng.integers(-8, 9, size=(k, n))           # K x N as on the page
+    A = synth.to_bf16(ai.astype(np.float32))
+    Bt = synth.to_bf16(bi.T.copy().astype(np.float32))  # stored N x K
+    v, bound = oracle.gemm(m, n, k, A, k, Bt, k)
+    ref = ai @ bi
+    assert v.shape == (16, 8) and ref.size == int(facts["outputs"][0])
+    assert np.array_equal(v, ref.astype(np.float64))
+    assert np.array_equal(bound, (np.abs(ai)[:, :, None] * np.abs(bi)[None]).sum(1))
+
+
+def test_fragment_lane_facts_agree_between_the_two_pages():
+    facts = _golden("mma_m16n8k16_example.txt")
+    for r in facts:
+        if r[0] == "lane_of":
+            row, col, lane = map(int, r[1:])
+            assert 4 * (row % 8) + col // 2 == lane
+        if r[0] == "lane_holds":
+            lane = int(r[1])
+            held = {tuple(map(int, x.split(","))) for x in r[2:]}
+            assert held == {(row, col) for row in range(16) for col in range(8)
+                            if 4 * (row % 8) + col // 2 == lane}
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_bf16_brute_force_tiny_shapes(seed):
+    rng = random.Random(seed)
+    M, N, K = rng.randint(1, 9), rng.randint(1, 9), rng.randint(1, 20)
+    lda, ldb, ldc = K + rng.randint(0, 3), K + rng.randint(0, 3), N + rng.randint(0, 2)
+    A = synth.bf16(seed, 1, M, K, ld=lda, dist="uniform", p0=-1, p1=1).ravel()
+    B = synth.bf16(seed, 2, N, K, ld=ldb, dist="uniform", p0=-1, p1=1).ravel()
+    C = synth.values_f32(seed, 3, M, ldc).ravel()
+    alpha, beta = 0.75, -1.5
+    v, bound = oracle.gemm(M, N, K, A, lda, B, ldb, C=C, ldc=ldc, c_type=oracle.C_F32,
+                           alpha=alpha, beta=beta)
+    a = _frac_rows(oracle.bf16_decode(A), M, K, lda)
+    b = _frac_rows(oracle.bf16_decode(B), N, K, ldb)
+    c = _frac_rows(C.astype(np.float64), M, N, ldc)
+    ex = _exact_gemm(M, N, K, a, b, alpha, beta, c)
+    for i in range(M):
+        for j in range(N):
+            bnd = sum(abs(a[i][k] * b[j][k]) for k in range(K)) * Fraction(alpha)
+            assert abs(Fraction(v[i, j]) - ex[i][j]) <= Fraction(K + 2, 2 ** 52) * (
+                bnd + abs(c[i][j]) * 2)
+            assert Fraction(bound[i, j]) == bnd  # exact: few 16-bit products
+
+
+def test_fp8_block_scale_indexing_exact():
+    """Block mode with power-of-two scales: every index error changes bits."""
+    M, N, K = 5, 260, 300
+    KB, NB = (K + 127) // 128, (N + 127) // 128
+    rng = np.random.default_rng(7)
+    qa = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+    qb = rng.integers(0, 256, size=(N, K)).astype(np.uint8)
+    qa[(qa & 0x7F) >= 0x78] = 0x38  # avoid NaN codes and huge values
+    qb[(qb & 0x7F) >= 0x78] = 0x40
+    sa = np.array([2.0 ** ((i % 7) - 3 + (kb % 5)) for kb in range(KB) for i in range(M)],
+                  dtype=np.float32)
+    sb = np.array([2.0 ** ((nb + kb) % 4) for nb in range(NB) for kb in range(KB)],
+                  dtype=np.float32)
+    v, _ = oracle.gemm(M, N, K, qa, K, qb, K, in_type=oracle.IN_E4M3,
+                       scale_mode=oracle.SCALE_BLOCK128, a_scale=sa, b_scale=sb)
+    a = _frac_rows(oracle.e4m3_decode(qa.ravel()), M, K, K)
+    b = _frac_rows(oracle.e4m3_decode(qb.ravel()), N, K, K)
+    ex = _exact_gemm(M, N, K, a, b, sa=sa, sb=sb, block=True)
+    for i in range(M):
+        for j in range(N):
+            assert Fraction(v[i, j]) == ex[i][j], (i, j)
+
+
+def test_fp8_tensor_scale_exact():
+    M, N, K = 4, 6, 64
+    rng = np.random.default_rng(8)
+    qa = rng.integers(0, 0x77, size=(M, K)).astype(np.uint8) | (rng.integers(0, 2, (M, K)) << 7).astype(np.uint8)
+    qb = rng.integers(0, 0x77, size=(N, K)).astype(np.uint8)
+    sa, sb = np.array([2.0 ** -3], np.float32), np.array([2.0 ** 5], np.float32)
+    v, _ = oracle.gemm(M, N, K, qa, K, qb, K, in_type=oracle.IN_E4M3,
+                       scale_mode=oracle.SCALE_TENSOR, a_scale=sa, b_scale=sb)
+    a = _frac_rows(oracle.e4m3_decode(qa.ravel()), M, K, K)
+    b = _frac_rows(oracle.e4m3_decode(qb.ravel()), N, K, K)
+    ex = _exact_gemm(M, N, K, a, b, sa=sa, sb=sb)
+    assert all(Fraction(v[i, j]) == ex[i][j] for i in range(M) for j in range(N))
+
+
+# ------------------------------------------------------------ closed forms
+
+def test_identity_gives_b_transposed_exactly():
+    n, N = 48, 37
+    A = synth.to_bf16(np.eye(n, dtype=np.float32))
+    B = synth.bf16(3, 2, N, n)                     # N x K
+    v, _ = oracle.gemm(n, N, n, A, n, B, n)
+    assert np.array_equal(v, oracle.bf16_decode(B).reshape(N, n).T)
+
+
+@pytest.mark.parametrize("K", [1, 7, 128, 1000, 8192])
+def test_all_ones_equals_k(K):
+    M, N = 3, 5
+    ones = synth.to_bf16(np.ones((max(M, N), K), np.float32))
+    v, bound = oracle.gemm(M, N, K, ones[:M], K, ones[:N], K)
+    assert (v == K).all() and (bound == K).all()
+    q = np.full((max(M, N), K), 0x38, np.uint8)    # E4M3 1.0
+    sa, sb = np.array([2.0 ** 3], np.float32), np.array([2.0 ** -5], np.float32)
+    v8, _ = oracle.gemm(M, N, K, q[:M], K, q[:N], K, in_type=oracle.IN_E4M3,
+                        scale_mode=oracle.SCALE_TENSOR, a_scale=sa, b_scale=sb)
+    assert (v8 == K * 2.0 ** -2).all()
+
+
+def test_alpha_beta_closed_form_and_k_zero():
+    M, N, K = 4, 6, 32
+    ones = synth.to_bf16(np.ones((8, K), np.float32))
+    cvals = np.arange(M * N, dtype=np.float32).reshape(M, N) - 7
+    Cb = synth.to_bf16(cvals)
+    v, _ = oracle.gemm(M, N, K, ones, K, ones, K, C=Cb, ldc=N, c_type=oracle.C_BF16,
+                       alpha=0.5, beta=-2.0)
+    assert np.array_equal(v, 0.5 * K - 2.0 * cvals)
+    v0, b0 = oracle.gemm(M, N, 0, ones, K, ones, K, C=Cb, ldc=N, c_type=oracle.C_BF16,
+                         alpha=3.0, beta=1.0)
+    assert np.array_equal(v0, cvals) and (b0 == 0).all()
+
+
+def test_beta_zero_ignores_c_even_nan():
+    M, N, K = 2, 3, 4
+    ones = synth.to_bf16(np.ones((4, K), np.float32))
+    C = np.full(M * N, np.nan, np.float32)
+    v, _ = oracle.gemm(M, N, K, ones, K, ones, K, C=C, ldc=N, beta=0.0)
+    assert (v == K).all()
+
+
+def test_tiles_match_whole_output_and_thread_count():
+    M, N, K = 70, 90, 50
+    A = synth.bf16(11, 1, M, K)
+    B = synth.bf16(11, 2, N, K)
+    full, fb = oracle.gemm(M, N, K, A, K, B, K, nthreads=1)
+    tiles = [(0, 0, 16, 16), (64, 80, 6, 10), (5, 7, 1, 1), (10, 0, 60, 90)]
+    vs, bs = oracle.gemm(M, N, K, A, K, B, K, tiles=tiles, nthreads=3)
+    for (i0, j0, mi, nj), v, b in zip(tiles, vs, bs):
+        assert np.array_equal(v, full[i0:i0 + mi, j0:j0 + nj])
+        assert np.array_equal(b, fb[i0:i0 + mi, j0:j0 + nj])
+
+
+def test_output_cast_is_nearest_even_of_fp32():
+    # the value goes through FP32 first (the kernel's accumulator type): a
+    # difference below FP32's precision is lost before the BF16 rounding
+    v = np.array([1.0, 1 + 2 ** -8, 1 + 2 ** -8 + 2 ** -20, 1 + 2 ** -8 + 2 ** -30,
+                  -3.0e38 * 10, 0.0], np.float64)
+    got = oracle.bf16_decode(oracle.cast_bf16(v))
+    assert got[0] == 1.0 and got[1] == 1.0 and got[2] == 1.0 + 2 ** -7 and got[3] == 1.0
+    assert np.isinf(got[4]) and got[4] < 0 and got[5] == 0.0
+
+
+def test_flop_formula_matches_the_pages():
+    for M, N, K, f in _golden("flop_counts.txt"):
+        flops = 2 * int(M) * int(N) * int(K)
+        if "e9" in f:
+            assert round(flops / 1e9, 1) == float(f) / 1e9
+        else:
+            assert flops == int(f)
+
+
+def test_bf16_error_bound_sanity_against_float32_gemm():
+    """An FP32 GEMM of the same inputs sits inside the BF16 tolerance of the
+    oracle, and a one-ulp perturbation of a large entry is caught by it."""
+    M, N, K = 64, 64, 512
+    A = synth.bf16(2, 1, M, K)
+    B = synth.bf16(2, 2, N, K)
+    v, bound = oracle.gemm(M, N, K, A, K, B, K)
+    af = oracle.bf16_decode(A).reshape(M, K).astype(np.float32)
+    bf = oracle.bf16_decode(B).reshape(N, K).astype(np.float32)
+    d32 = (torch.from_numpy(af) @ torch.from_numpy(bf).T).double().numpy()
+    tol = 2.0 ** -14 * bound + 1e-6
+    assert (np.abs(d32 - v) <= tol).all()
+    bad = d32.copy()
+    i, j = np.unravel_index(np.argmax(np.abs(v)), v.shape)
+    bad[i, j] = v[i, j] + 2 * tol[i, j]
+    assert not (np.abs(bad - v) <= tol).all()
+    assert math.isfinite(float(v.sum()))
