@@ -1,0 +1,128 @@
+/*
+ * tcgemm.h -- dense tensor-core GEMM for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ *     D = alpha * A * B + beta * C          (FP32 accumulation)
+ *
+ * The operation is the matrix multiply-accumulate D = A*B + C, A M x K, B
+ * K x N, C and D M x N ("Tensor Cores: Matrix Instructions, Swizzling and
+ * FP8, Measured", Step 1), on BF16 operands ("Tensor Cores", "Precision:
+ * FP16, BF16, TF32, FP8") or FP8 E4M3 operands carrying FP32 scale factors
+ * that are removed after the product ("Tensor cores and low precision", the
+ * FP8 scaling paragraph).
+ *
+ * Layouts (all row-major with an explicit leading dimension, in elements):
+ *   A  M x K, element (i, k) at A[i * lda + k]            (K contiguous)
+ *   B  stored N x K, element (k, j) at B[j * ldb + k]     (K contiguous; the
+ *      "TN" layout of the 4,096^3 test in the page above, Step 2)
+ *   C  M x N, (i, j) at C[i * ldc + j]; same dtype as D; read only if beta != 0
+ *   D  M x N, (i, j) at D[i * ldd + j]; BF16 (round to nearest even) or FP32
+ *
+ * Every pointer is a device pointer owned by the caller.  A call enqueues
+ * work on `stream` and returns without synchronising; D is valid once the
+ * stream has reached that point.  The library allocates no memory per call:
+ * it keeps a process-wide cache of TMA tensor maps (host memory) and, for the
+ * split-K skinny path of gemm_fp8_e4m3, a per-device workspace that is
+ * allocated on first use and grown when a larger one is needed (that first
+ * call therefore must not be made during stream capture).  Calls on
+ * different streams may run concurrently, except that calls sharing that
+ * workspace are serialised by the stream order the caller gives them; two
+ * concurrent skinny calls on different streams of one device race on it.
+ *
+ * No exception or abort crosses this boundary: every entry point returns a
+ * tcg_status.  Argument errors are detected on the host before anything is
+ * enqueued.  A device-side wait that exceeds its time limit (which would
+ * indicate a bug, never a slow GPU) makes the kernel exit early and records
+ * TCG_ERR_TIMEOUT in a device status word read by tcg_last_device_status().
+ */
+#ifndef TCGEMM_H
+#define TCGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* tcg_stream;
+
+typedef enum {
+  TCG_OK = 0,
+  TCG_ERR_INVALID_ARG = 1, /* negative size, ld too small, NULL pointer, ... */
+  TCG_ERR_ALIGNMENT = 2,   /* base not 16-byte aligned or row pitch not a multiple of 16 bytes */
+  TCG_ERR_UNSUPPORTED = 3, /* an enum value or size this library does not handle */
+  TCG_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+  TCG_ERR_TIMEOUT = 5      /* a device-side wait ran out (reported by tcg_last_device_status) */
+} tcg_status;
+
+typedef enum { TCG_OUT_BF16 = 0, TCG_OUT_F32 = 1 } tcg_out_dtype;
+
+typedef enum {
+  /* a_scale[0] and b_scale[0]: one FP32 scale per operand */
+  TCG_SCALE_TENSOR = 0,
+  /* one FP32 scale per 1 x 128 block of A (row i, K block kb) at
+   * a_scale[kb * M + i], and per 128 x 128 block of B (N block nb, K block
+   * kb) at b_scale[nb * ceil(K/128) + kb] */
+  TCG_SCALE_BLOCK128 = 1
+} tcg_scale_mode;
+
+/*
+ * gemm_bf16 -- D = alpha * A * B + beta * C with BF16 A and B.
+ *
+ * M, N, K      sizes, >= 0.  M == 0 or N == 0: nothing is done.  K == 0:
+ *              D = beta * C (zero when beta == 0).
+ * A, lda       BF16, M x K, lda >= K.  B, ldb: BF16, N x K, ldb >= K.
+ * C, ldc       dtype given by out_dtype; may be NULL iff beta == 0; ldc >= N.
+ *              C may alias D only exactly (C == D and ldc == ldd).
+ * D, ldd       out_dtype, M x N, ldd >= N.
+ * Alignment    A, B, C, D 16-byte aligned; lda*2, ldb*2, ldc*size, ldd*size
+ *              multiples of 16 bytes (a TMA requirement for A and B; vector
+ *              stores for C and D).
+ * Numerics     products accumulate in FP32 on the tensor cores; alpha and beta
+ *              are applied in FP32; BF16 output rounds to nearest even.
+ */
+tcg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                     int64_t ldb, const void* C, int64_t ldc, void* D, int64_t ldd,
+                     tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream);
+
+/*
+ * gemm_fp8_e4m3 -- D = alpha * (sA . A) * (sB . B) + beta * C with E4M3 bytes
+ * in A and B and FP32 dequantisation scales (device pointers).
+ *
+ * Layouts and alignment as gemm_bf16 with one byte per element of A and B
+ * (lda, ldb multiples of 16).  mode selects the scale granularity above; the
+ * scales must be finite.
+ * TCG_SCALE_TENSOR   the per-tensor product a_scale[0]*b_scale[0]*alpha is
+ *                    applied once, in the epilogue.
+ * TCG_SCALE_BLOCK128 every 128-wide K block is accumulated on its own and
+ *                    promoted into an FP32 register accumulator with its
+ *                    scales sa[i,kb] * sb[j/128,kb] ("promotion": partial sums
+ *                    moved to FP32 at intervals, "Tensor Cores: Matrix
+ *                    Instructions, Swizzling and FP8, Measured", Step 5).
+ *                    Supported for M <= 128 (the skinny/decode shape); larger
+ *                    M returns TCG_ERR_UNSUPPORTED.
+ */
+tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, const float* a_scale, const float* b_scale,
+                         tcg_scale_mode mode, const void* C, int64_t ldc, void* D, int64_t ldd,
+                         tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream);
+
+/* A static, human-readable name for a status code. */
+const char* tcg_status_string(tcg_status status);
+
+/*
+ * Synchronises `stream`, then reads and clears this device's status word.
+ * Returns TCG_ERR_TIMEOUT if any kernel of this library on the current
+ * device gave up on a wait since the last call, TCG_ERR_CUDA if the
+ * synchronisation failed, else TCG_OK.  Meant for tests and debugging.
+ */
+tcg_status tcg_last_device_status(tcg_stream stream);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t tcg_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCGEMM_H */

@@ -1,0 +1,169 @@
+"""Python binding for libtcgemm.so, the sm_103a tensor-core GEMM library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI of ``include/tcgemm.h``.  PyTorch provides device
+memory and streams.  There is no CPU fallback: if the compiled library is
+missing, importing the binding's entry points raises.
+
+    D = alpha * A @ B.T + beta * C      (A: M x K, B: N x K, both K-major)
+
+The entry points keep the C names: ``gemm_bf16`` and ``gemm_fp8_e4m3``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libtcgemm.so")
+
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
+OUT_BF16, OUT_F32 = 0, 1
+SCALE_TENSOR, SCALE_BLOCK128 = 0, 1
+
+# Every symbol include/tcgemm.h declares.
+EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "tcg_status_string", "tcg_last_device_status",
+           "tcg_launch_count")
+
+_lib = None
+
+
+class TcgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with tensor_core_dense_gb300.build.build() "
+                "(or __graft_entry__.build()); there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, vp, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+        L.gemm_bf16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, f32, f32,
+                                vp]
+        L.gemm_bf16.restype = i32
+        L.gemm_fp8_e4m3.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, vp, i32, vp, i64, vp,
+                                    i64, i32, f32, f32, vp]
+        L.gemm_fp8_e4m3.restype = i32
+        L.tcg_status_string.argtypes = [i32]
+        L.tcg_status_string.restype = ctypes.c_char_p
+        L.tcg_last_device_status.argtypes = [vp]
+        L.tcg_last_device_status.restype = i32
+        L.tcg_launch_count.argtypes = []
+        L.tcg_launch_count.restype = ctypes.c_uint64
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().tcg_status_string(int(status)).decode()
+
+
+def launch_count() -> int:
+    """Kernels launched by the library in this process."""
+    return int(lib().tcg_launch_count())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return getattr(stream, "cuda_stream", stream) or None
+
+
+def last_device_status(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status word."""
+    return int(lib().tcg_last_device_status(_stream_handle(stream)))
+
+
+# ------------------------------------------------------------ raw entry points
+
+def gemm_bf16_raw(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, out_dtype, alpha, beta,
+                  stream) -> int:
+    """The C call with integer device pointers; returns the status code."""
+    return int(lib().gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, out_dtype,
+                               float(alpha), float(beta), stream))
+
+
+def gemm_fp8_e4m3_raw(M, N, K, A, lda, B, ldb, a_scale, b_scale, mode, C, ldc, D, ldd,
+                      out_dtype, alpha, beta, stream) -> int:
+    return int(lib().gemm_fp8_e4m3(M, N, K, A, lda, B, ldb, a_scale, b_scale, mode, C, ldc, D,
+                                   ldd, out_dtype, float(alpha), float(beta), stream))
+
+
+# --------------------------------------------------------------- tensor API
+
+def _ld(t, rows_name):
+    """Leading dimension in elements.  A single-row matrix never uses its row
+    pitch, so it gets the smallest 16-byte-multiple pitch >= its width."""
+    if t.dim() != 2:
+        raise ValueError(f"{rows_name} must be 2-D")
+    if t.size(1) > 1 and t.stride(1) != 1:
+        raise ValueError(f"{rows_name} must have a contiguous last dimension")
+    if t.size(0) > 1:
+        return t.stride(0)
+    step = max(1, 16 // t.element_size())
+    return max(step, -(-t.size(1) // step) * step)
+
+
+def _out_dtype(D):
+    import torch
+    if D.dtype == torch.bfloat16:
+        return OUT_BF16
+    if D.dtype == torch.float32:
+        return OUT_F32
+    raise ValueError("D must be bfloat16 or float32")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def gemm_bf16(A, B, D, C=None, *, alpha=1.0, beta=0.0, stream=None):
+    """D = alpha * A @ B.T + beta * C on the GPU (BF16 A, B; D/C BF16 or FP32)."""
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise ValueError("A and B must be bfloat16")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    if C is not None and (tuple(C.shape) != (M, N) or C.dtype != D.dtype):
+        raise ValueError("C must match D")
+    st = gemm_bf16_raw(M, N, K, _ptr(A), _ld(A, "A"), _ptr(B), _ld(B, "B"), _ptr(C),
+                       _ld(C, "C") if C is not None else 0, _ptr(D), _ld(D, "D"), _out_dtype(D),
+                       alpha, beta if C is not None else 0.0, _stream_handle(stream))
+    if st != OK:
+        raise TcgError(st, "gemm_bf16")
+    return D
+
+
+def gemm_fp8_e4m3(A, B, a_scale, b_scale, D, C=None, *, mode=SCALE_TENSOR, alpha=1.0,
+                  beta=0.0, stream=None):
+    """D = alpha * (sa.A) @ (sb.B).T + beta * C with E4M3 A, B (uint8 or float8_e4m3fn)
+    and FP32 scale tensors on the device (layouts in include/tcgemm.h)."""
+    import torch
+    for t, n in ((A, "A"), (B, "B")):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise ValueError(f"{n} must hold E4M3 bytes")
+    if a_scale.dtype != torch.float32 or b_scale.dtype != torch.float32:
+        raise ValueError("scales must be float32")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    if C is not None and (tuple(C.shape) != (M, N) or C.dtype != D.dtype):
+        raise ValueError("C must match D")
+    st = gemm_fp8_e4m3_raw(M, N, K, _ptr(A), _ld(A, "A"), _ptr(B), _ld(B, "B"), _ptr(a_scale),
+                           _ptr(b_scale), mode, _ptr(C), _ld(C, "C") if C is not None else 0,
+                           _ptr(D), _ld(D, "D"), _out_dtype(D), alpha,
+                           beta if C is not None else 0.0, _stream_handle(stream))
+    if st != OK:
+        raise TcgError(st, "gemm_fp8_e4m3")
+    return D

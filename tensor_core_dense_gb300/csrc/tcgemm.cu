@@ -1,0 +1,418 @@
+// tcgemm.cu -- host side of the C ABI declared in include/tcgemm.h:
+// argument validation, TMA tensor-map encoding (cached), kernel selection and
+// launch.  The kernels themselves are in gemm_tn.cuh (large shapes, BF16 and
+// per-tensor FP8) and gemm_skinny.cuh (block-scaled FP8, M <= 128).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "gemm_skinny.cuh"
+#include "gemm_tn.cuh"
+#include "tcgemm.h"
+
+namespace tcg {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// ---------------------------------------------------------------- K == 0
+
+// D = beta * C (or 0): the product has no terms.
+__global__ void scale_c_kernel(int64_t M, int64_t N, const void* C, int64_t ldc, void* D,
+                               int64_t ldd, float beta, int out_f32, int has_c) {
+  const int64_t total = M * N;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = e / N, j = e % N;
+    float v = 0.0f;
+    if (out_f32) {
+      if (has_c) v = beta * static_cast<const float*>(C)[i * ldc + j];
+      static_cast<float*>(D)[i * ldd + j] = v;
+    } else {
+      if (has_c)
+        v = beta * __uint_as_float((uint32_t)static_cast<const uint16_t*>(C)[i * ldc + j] << 16);
+      static_cast<uint16_t*>(D)[i * ldd + j] = (uint16_t)(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- devices
+
+struct DeviceInfo {
+  int sms = 0;
+  bool init = false;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+tcg_status current_device(int* dev, int* sms) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return TCG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[*dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess)
+      return TCG_ERR_CUDA;
+    d.init = true;
+  }
+  *sms = d.sms;
+  return TCG_OK;
+}
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device).
+std::mutex g_attr_mu;
+std::unordered_map<uint64_t, bool> g_attr_done;
+
+template <typename F>
+tcg_status ensure_smem(F* fn, uint32_t bytes, int dev) {
+  const uint64_t key = (uint64_t)(uintptr_t)fn * 131u + (uint64_t)dev;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (g_attr_done.count(key)) return TCG_OK;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)bytes) != cudaSuccess)
+    return TCG_ERR_CUDA;
+  g_attr_done[key] = true;
+  return TCG_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  uint64_t ptr, inner, rows, ld_bytes;
+  uint32_t dtype, box_inner, box_rows;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && inner == o.inner && rows == o.rows && ld_bytes == o.ld_bytes &&
+           dtype == o.dtype && box_inner == o.box_inner && box_rows == o.box_rows;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = 1469598103934665603ull;
+    const uint64_t v[7] = {k.ptr, k.inner, k.rows, k.ld_bytes, k.dtype, k.box_inner, k.box_rows};
+    for (uint64_t x : v) h = (h ^ x) * 1099511628211ull;
+    return (size_t)h;
+  }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+constexpr size_t kMaxCachedMaps = 4096;
+
+// A 2-D row-major matrix (rows x inner elements, pitch ld_bytes) read in
+// boxes of box_rows x box_inner with 128-byte swizzling; out-of-range
+// elements read as zero.
+tcg_status tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, const void* ptr,
+                      uint64_t inner, uint64_t rows, uint64_t ld_bytes, uint32_t box_inner,
+                      uint32_t box_rows) {
+  const MapKey key{(uint64_t)(uintptr_t)ptr, inner, rows, ld_bytes, (uint32_t)dtype, box_inner,
+                   box_rows};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return TCG_OK;
+    }
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return TCG_ERR_CUDA;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof m);
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {ld_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return TCG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+  g_maps.emplace(key, m);
+  *out = m;
+  return TCG_OK;
+}
+
+// ---------------------------------------------------- skinny workspace
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+Workspace g_ws[kMaxDevices];
+std::mutex g_ws_mu;
+
+// Per-device workspace: counters (n_tiles words, kept zero between calls)
+// followed by the FP32 partial slots.  Grown on demand, never shrunk.
+tcg_status get_workspace(int dev, size_t counter_bytes, size_t partial_bytes, cudaStream_t stream,
+                         unsigned int** counters, float** partials) {
+  const size_t cbytes = (counter_bytes + 255) & ~size_t(255);
+  const size_t need = cbytes + partial_bytes;
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  Workspace& w = g_ws[dev];
+  if (w.bytes < need) {
+    if (w.ptr) {
+      if (cudaDeviceSynchronize() != cudaSuccess) return TCG_ERR_CUDA;
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, need) != cudaSuccess) return TCG_ERR_CUDA;
+    // counters must start at zero; the region past the old size is new
+    if (cudaMemsetAsync(p, 0, need, stream) != cudaSuccess) {
+      cudaFree(p);
+      return TCG_ERR_CUDA;
+    }
+    w.ptr = p;
+    w.bytes = need;
+  }
+  *counters = static_cast<unsigned int*>(w.ptr);
+  *partials = reinterpret_cast<float*>(static_cast<char*>(w.ptr) + cbytes);
+  return TCG_OK;
+}
+
+// ------------------------------------------------------------- validation
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct Common {
+  int64_t M, N, K;
+  const void *A, *B, *C;
+  int64_t lda, ldb, ldc, ldd;
+  void* D;
+  int out;  // tcg_out_dtype
+  float alpha, beta;
+};
+
+// Checks shared by both entry points; in_bytes = bytes per A/B element.
+tcg_status validate(const Common& a, int in_bytes) {
+  if (a.M < 0 || a.N < 0 || a.K < 0) return TCG_ERR_INVALID_ARG;
+  if (a.out != TCG_OUT_BF16 && a.out != TCG_OUT_F32) return TCG_ERR_UNSUPPORTED;
+  if (a.M == 0 || a.N == 0) return TCG_OK;
+  if (a.M > INT32_MAX || a.N > INT32_MAX || a.K > INT32_MAX) return TCG_ERR_UNSUPPORTED;
+  const int out_bytes = a.out == TCG_OUT_F32 ? 4 : 2;
+  if (!a.D || a.ldd < a.N) return TCG_ERR_INVALID_ARG;
+  if (a.beta != 0.0f && (!a.C || a.ldc < a.N)) return TCG_ERR_INVALID_ARG;
+  if (a.K > 0 && (!a.A || !a.B || a.lda < a.K || a.ldb < a.K)) return TCG_ERR_INVALID_ARG;
+  if (!aligned16(a.D) || (a.ldd * out_bytes) % 16 != 0) return TCG_ERR_ALIGNMENT;
+  if (a.beta != 0.0f && (!aligned16(a.C) || (a.ldc * out_bytes) % 16 != 0))
+    return TCG_ERR_ALIGNMENT;
+  if (a.K > 0 && (!aligned16(a.A) || !aligned16(a.B) || (a.lda * in_bytes) % 16 != 0 ||
+                  (a.ldb * in_bytes) % 16 != 0))
+    return TCG_ERR_ALIGNMENT;
+  return TCG_OK;
+}
+
+tcg_status launch_k0(const Common& a, cudaStream_t stream) {
+  const int64_t total = a.M * a.N;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int blocks = (int)(want < 4096 ? want : 4096);
+  scale_c_kernel<<<blocks, threads, 0, stream>>>(a.M, a.N, a.beta != 0.0f ? a.C : nullptr, a.ldc,
+                                                 a.D, a.ldd, a.beta, a.out == TCG_OUT_F32,
+                                                 a.beta != 0.0f);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+template <int kIn, int kOut, bool kHasC>
+tcg_status launch_tn_inst(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
+                          int grid, int dev, cudaStream_t stream) {
+  auto* fn = &gemm_tn_kernel<kIn, kOut, kHasC>;
+  if (tcg_status s = ensure_smem(fn, kSmemBytes, dev); s != TCG_OK) return s;
+  fn<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+// The persistent 128 x 256 tile kernel (BF16, or per-tensor FP8).
+template <int kIn>
+tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale,
+                     cudaStream_t stream) {
+  int dev, sms;
+  if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+  const int in_bytes = kIn == 0 ? 2 : 1;
+  const CUtensorMapDataType dt =
+      kIn == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint32_t box_k = kBKBytes / in_bytes;
+  CUtensorMap ma, mb;
+  if (tcg_status s = tensor_map(&ma, dt, a.A, a.K, a.M, a.lda * in_bytes, box_k, kBM); s != TCG_OK)
+    return s;
+  if (tcg_status s = tensor_map(&mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, box_k, kBN); s != TCG_OK)
+    return s;
+  GemmParams p{};
+  p.M = (int32_t)a.M;
+  p.N = (int32_t)a.N;
+  p.K = (int32_t)a.K;
+  p.tiles_m = (int32_t)((a.M + kBM - 1) / kBM);
+  p.tiles_n = (int32_t)((a.N + kBN - 1) / kBN);
+  p.num_kb = (int32_t)((a.K * in_bytes + kBKBytes - 1) / kBKBytes);
+  const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+  if (tiles > INT32_MAX) return TCG_ERR_UNSUPPORTED;
+  p.num_tiles = (int32_t)tiles;
+  p.C = a.beta != 0.0f ? a.C : nullptr;
+  p.ldc = a.ldc;
+  p.D = a.D;
+  p.ldd = a.ldd;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.a_scale = a_scale;
+  p.b_scale = b_scale;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  const bool has_c = a.beta != 0.0f;
+  if (a.out == TCG_OUT_BF16)
+    return has_c ? launch_tn_inst<kIn, 0, true>(ma, mb, p, grid, dev, stream)
+                 : launch_tn_inst<kIn, 0, false>(ma, mb, p, grid, dev, stream);
+  return has_c ? launch_tn_inst<kIn, 1, true>(ma, mb, p, grid, dev, stream)
+               : launch_tn_inst<kIn, 1, false>(ma, mb, p, grid, dev, stream);
+}
+
+template <int kMp>
+tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
+                              cudaStream_t stream, int dev, int sms) {
+  using Cfg = SkinnyCfg<kMp>;
+  CUtensorMap ma, mb;
+  if (tcg_status s = tensor_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.lda, 128, kMp);
+      s != TCG_OK)
+    return s;
+  if (tcg_status s = tensor_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.ldb, 128, 128);
+      s != TCG_OK)
+    return s;
+  SkinnyParams p{};
+  p.M = (int32_t)a.M;
+  p.N = (int32_t)a.N;
+  p.K = (int32_t)a.K;
+  p.n_tiles = (int32_t)((a.N + 127) / 128);
+  p.num_kb = (int32_t)((a.K + 127) / 128);
+  const int64_t T = (int64_t)p.n_tiles * p.num_kb;
+  if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
+  p.total_steps = (int32_t)T;
+  p.grid = (int32_t)(T < sms ? T : sms);
+  // Segments per tile: a tile of num_kb steps meets at most
+  // ceil(num_kb / min_range) + 1 ranges, min_range = floor(T / grid).
+  const int64_t min_range = T / p.grid;
+  p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);
+  if (p.max_seg > p.grid) p.max_seg = p.grid;
+  p.a_scale = sa;
+  p.b_scale = sb;
+  p.C = a.beta != 0.0f ? a.C : nullptr;
+  p.ldc = a.ldc;
+  p.D = a.D;
+  p.ldd = a.ldd;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.out_f32 = a.out == TCG_OUT_F32;
+  p.has_c = a.beta != 0.0f;
+  if (p.num_kb > 1) {  // a tile may be split over CTAs: needs the workspace
+    const size_t partial_bytes = (size_t)p.n_tiles * p.max_seg * kMp * 128 * sizeof(float);
+    if (tcg_status s = get_workspace(dev, (size_t)p.n_tiles * sizeof(unsigned int),
+                                     partial_bytes, stream, &p.counters, &p.ws);
+        s != TCG_OK)
+      return s;
+  }
+  auto* fn = &gemm_fp8_block_skinny_kernel<kMp>;
+  if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
+  fn<<<p.grid, kSkThreads, Cfg::kSmemBytes, stream>>>(ma, mb, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, cudaStream_t stream) {
+  int dev, sms;
+  if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+  if (a.M <= 16) return launch_skinny_inst<16>(a, sa, sb, stream, dev, sms);
+  if (a.M <= 32) return launch_skinny_inst<32>(a, sa, sb, stream, dev, sms);
+  if (a.M <= 64) return launch_skinny_inst<64>(a, sa, sb, stream, dev, sms);
+  return launch_skinny_inst<128>(a, sa, sb, stream, dev, sms);
+}
+
+}  // namespace
+}  // namespace tcg
+
+using namespace tcg;
+
+extern "C" {
+
+tcg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                     int64_t ldb, const void* C, int64_t ldc, void* D, int64_t ldd,
+                     tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream) {
+  const Common a{M, N, K, A, B, C, lda, ldb, ldc, ldd, D, (int)out_dtype, alpha, beta};
+  if (tcg_status s = validate(a, 2); s != TCG_OK) return s;
+  if (M == 0 || N == 0) return TCG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_k0(a, st);
+  return launch_tn<0>(a, nullptr, nullptr, st);
+}
+
+tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, const float* a_scale, const float* b_scale,
+                         tcg_scale_mode mode, const void* C, int64_t ldc, void* D, int64_t ldd,
+                         tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream) {
+  const Common a{M, N, K, A, B, C, lda, ldb, ldc, ldd, D, (int)out_dtype, alpha, beta};
+  if (mode != TCG_SCALE_TENSOR && mode != TCG_SCALE_BLOCK128) return TCG_ERR_UNSUPPORTED;
+  if (tcg_status s = validate(a, 1); s != TCG_OK) return s;
+  if (M == 0 || N == 0) return TCG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_k0(a, st);
+  if (!a_scale || !b_scale) return TCG_ERR_INVALID_ARG;
+  if (mode == TCG_SCALE_TENSOR) return launch_tn<1>(a, a_scale, b_scale, st);
+  if (M > 128) return TCG_ERR_UNSUPPORTED;
+  return launch_skinny(a, a_scale, b_scale, st);
+}
+
+const char* tcg_status_string(tcg_status status) {
+  switch (status) {
+    case TCG_OK: return "ok";
+    case TCG_ERR_INVALID_ARG: return "invalid argument";
+    case TCG_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+    case TCG_ERR_UNSUPPORTED: return "unsupported argument";
+    case TCG_ERR_CUDA: return "CUDA error";
+    case TCG_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+tcg_status tcg_last_device_status(tcg_stream stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TCG_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tcg_status, sizeof v) != cudaSuccess) return TCG_ERR_CUDA;
+  if (v == 0) return TCG_OK;
+  if (cudaMemcpyToSymbol(g_tcg_status, &zero, sizeof zero) != cudaSuccess) return TCG_ERR_CUDA;
+  // A timed-out split-K call may have left tile counters non-zero.
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (g_ws[dev].ptr) cudaMemset(g_ws[dev].ptr, 0, g_ws[dev].bytes);
+  }
+  return TCG_ERR_TIMEOUT;
+}
+
+uint64_t tcg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

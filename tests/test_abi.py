@@ -1,0 +1,86 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/tcgemm.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run on a machine with no GPU)."""
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"^(?:tcg_status|const char\*|uint64_t)\s+(\w+)\s*\(", text, re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def tcg():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from tensor_core_dense_gb300 import build
+    build.build()
+    import tensor_core_dense_gb300 as t
+    t.lib()
+    return t
+
+
+def test_exports_every_declared_symbol(tcg):
+    names = _declared()
+    assert set(names) >= {"gemm_bf16", "gemm_fp8_e4m3", "tcg_status_string",
+                          "tcg_last_device_status"}
+    raw = ctypes.CDLL(tcg.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(names) == set(tcg.EXPORTS)
+
+
+def test_status_strings(tcg):
+    for code in range(6):
+        assert tcg.status_string(code)
+    assert tcg.status_string(99) == "unknown status"
+
+
+A, B, C, D = 0x10000, 0x20000, 0x30000, 0x40000   # never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("args,want", [
+    ((-1, 8, 8, A, 8, B, 8, None, 0, D, 8, 0, 1.0, 0.0), 1),      # negative M
+    ((8, 8, 8, A, 4, B, 8, None, 0, D, 8, 0, 1.0, 0.0), 1),       # lda < K
+    ((8, 8, 8, A, 8, B, 8, None, 0, None, 8, 0, 1.0, 0.0), 1),    # D NULL
+    ((8, 8, 8, A, 8, B, 8, None, 0, D, 8, 0, 1.0, 1.0), 1),       # beta != 0 without C
+    ((8, 8, 8, None, 8, B, 8, None, 0, D, 8, 0, 1.0, 0.0), 1),    # A NULL
+    ((8, 8, 8, A + 2, 8, B, 8, None, 0, D, 8, 0, 1.0, 0.0), 2),   # A misaligned
+    ((8, 8, 12, A, 12, B, 16, None, 0, D, 8, 0, 1.0, 0.0), 2),    # lda*2 not 16-byte multiple
+    ((8, 9, 8, A, 8, B, 8, None, 0, D, 9, 0, 1.0, 0.0), 2),       # ldd*2 not 16-byte multiple
+    ((8, 8, 8, A, 8, B, 8, None, 0, D, 8, 7, 1.0, 0.0), 3),       # bad out dtype
+    ((0, 8, 8, None, 0, None, 0, None, 0, None, 0, 0, 1.0, 0.0), 0),  # empty: no-op
+    ((8, 0, 8, None, 0, None, 0, None, 0, None, 0, 0, 1.0, 0.0), 0),
+])
+def test_bf16_host_validation(tcg, args, want):
+    assert tcg.gemm_bf16_raw(*args, None) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((8, 8, 16, A, 16, B, 16, None, None, 0, None, 0, D, 8, 0, 1.0, 0.0), 1),  # no scales
+    ((8, 8, 16, A, 16, B, 16, A, B, 5, None, 0, D, 8, 0, 1.0, 0.0), 3),        # bad mode
+    ((8, 8, 24, A, 24, B, 32, A, B, 0, None, 0, D, 8, 0, 1.0, 0.0), 2),        # lda not x16
+    ((8, 8, 16, A, 8, B, 16, A, B, 0, None, 0, D, 8, 0, 1.0, 0.0), 1),         # lda < K
+])
+def test_fp8_host_validation(tcg, args, want):
+    assert tcg.gemm_fp8_e4m3_raw(*args, None) == want
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    import tensor_core_dense_gb300 as t
+    monkeypatch.setattr(t, "_lib", None)
+    monkeypatch.setattr(t, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        t.lib()

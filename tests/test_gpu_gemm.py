@@ -1,0 +1,270 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Small and ragged shapes are compared element by element on the whole output;
+the full-size workloads on seeded samples of 128 x 128 output tiles, in the
+same launch configuration the benchmark times.  Bit-exact cases use inputs
+whose products and sums are exact in FP32 (small integers, power-of-two
+scales), so any indexing or scale-placement error changes bits.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+import synth.workloads as W
+from helpers import (c_values, check_bf16, check_f32, d_to_host, oracle_for, run, sample_tiles,
+                     to_device)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import tensor_core_dense_gb300 as tcg
+    tcg.lib()
+    yield
+    assert tcg.last_device_status() == tcg.OK
+
+
+def _pad(n, step):
+    return -(-n // step) * step
+
+
+def bf16_case(M, N, K, seed, out="f32", alpha=1.0, beta=0.0, dist="normal"):
+    w = W.Workload(f"bf16_{M}x{N}x{K}", M, N, K, "bf16", out, alpha=alpha, beta=beta)
+    kw = dict(dist="uniform", p0=-1, p1=1) if dist == "uniform" else {}
+    w.A = synth.bf16(seed, 1, M, K, ld=_pad(K, 8), **kw)
+    w.B = synth.bf16(seed, 2, N, K, ld=_pad(K, 8), **kw)
+    if beta != 0.0:
+        if out == "bf16":
+            w.C = synth.bf16(seed, 3, M, N, ld=_pad(N, 8))
+        else:
+            w.C = np.zeros((M, _pad(N, 4)), np.float32)
+            w.C[:, :N] = synth.values_f32(seed, 3, M, N)
+    return w
+
+
+def fp8_case(M, N, K, seed, mode, out="f32", alpha=1.0, beta=0.0, outliers=0.0):
+    kind = "fp8_tensor" if mode == "tensor" else "fp8_block"
+    w = W.Workload(f"fp8_{mode}_{M}x{N}x{K}", M, N, K, kind, out, alpha=alpha, beta=beta)
+    xa = synth.values_f32(seed, 1, M, K, out_prob=outliers, out_factor=50.0)
+    xb = synth.values_f32(seed, 2, N, K, out_prob=outliers, out_factor=50.0)
+    if mode == "tensor":
+        w.A, w.a_scale = synth.e4m3_tensor(xa, ld=_pad(K, 16))
+        w.B, w.b_scale = synth.e4m3_tensor(xb, ld=_pad(K, 16))
+    else:
+        w.A, w.a_scale = synth.e4m3_rowblock(xa, ld=_pad(K, 16))
+        w.B, w.b_scale = synth.e4m3_block128(xb, ld=_pad(K, 16))
+    if beta != 0.0:
+        if out == "bf16":
+            w.C = synth.bf16(seed, 3, M, N, ld=_pad(N, 8))
+        else:
+            w.C = np.zeros((M, _pad(N, 4)), np.float32)
+            w.C[:, :N] = synth.values_f32(seed, 3, M, N)
+    return w
+
+
+def check_full(w, D):
+    v, bound = oracle_for(w)
+    got = d_to_host(D)[:, :w.N]
+    c = c_values(w.C)[:, :w.N] if w.C is not None else None
+    kind = "bf16" if w.kind == "bf16" else "fp8"
+    if got.dtype == np.uint16:
+        return check_bf16(kind, got, v, bound, w.beta, c, what=w.name)
+    return check_f32(kind, got, v, bound, w.beta, c, what=w.name)
+
+
+# ------------------------------------------------------------------ BF16
+
+def test_bf16_256_full_output():
+    """256^3, uniform [-1, 1), FP32 output, beta = 0: every output checked."""
+    w = W.make("bf16_256")
+    check_full(w, run(w))
+
+
+BF16_SHAPES = [(1, 1, 1), (1, 8, 8), (7, 13, 50), (128, 256, 64), (129, 257, 65),
+               (255, 511, 200), (300, 200, 1000), (64, 1000, 136), (1000, 48, 72),
+               (384, 768, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", BF16_SHAPES)
+@pytest.mark.parametrize("out,beta", [("f32", 0.0), ("bf16", 0.0), ("f32", -0.5), ("bf16", 1.0)])
+def test_bf16_shapes(M, N, K, out, beta):
+    w = bf16_case(M, N, K, seed=M * 7 + N * 3 + K, out=out, alpha=1.25 if beta else 1.0,
+                  beta=beta)
+    check_full(w, run(w))
+
+
+def test_bf16_one_hot_indexing_bit_exact():
+    """A has one 1 per row at column pi(i): the product is exactly B[j, pi(i)], so
+    D[i, j] = fp32(alpha * B[j, pi(i)] + beta * C[i, j]) bit for bit (alpha, beta
+    powers of two: the only rounding is the final FP32 sum), for padded
+    leading dimensions and ragged tiles."""
+    M, N, K = 333, 517, 700
+    lda, ldb = 712, 704
+    rng = np.random.default_rng(3)
+    pi = rng.integers(0, K, size=M)
+    a = np.zeros((M, lda), np.float32)
+    a[np.arange(M), pi] = 1.0
+    w = W.Workload("onehot", M, N, K, "bf16", "f32", alpha=2.0, beta=0.5)
+    w.A = synth.to_bf16(a)
+    w.B = synth.bf16(9, 2, N, K, ld=ldb)
+    w.C = np.zeros((M, 520), np.float32)
+    w.C[:, :N] = rng.integers(-64, 64, size=(M, N)).astype(np.float32)
+    got = d_to_host(run(w))[:, :N].astype(np.float64)
+    b = oracle.bf16_decode(w.B).reshape(N, ldb)
+    want = (2.0 * b[:, pi].T + 0.5 * w.C[:, :N]).astype(np.float32).astype(np.float64)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_all_ones_equals_k():
+    M, N, K = 130, 260, 4000
+    ones = synth.to_bf16(np.ones((max(M, N), K), np.float32))
+    w = W.Workload("ones", M, N, K, "bf16", "f32")
+    w.A, w.B = ones[:M], ones[:N]
+    assert (d_to_host(run(w)) == K).all()
+
+
+def test_k_zero_gives_beta_c():
+    import tensor_core_dense_gb300 as tcg
+    M, N = 37, 64
+    C = torch.randn(M, N, device="cuda")
+    D = torch.full((M, N), float("nan"), device="cuda")
+    A = torch.empty((M, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((N, 0), dtype=torch.bfloat16, device="cuda")
+    st = tcg.gemm_bf16_raw(M, N, 0, A.data_ptr(), 8, B.data_ptr(), 8, C.data_ptr(), N,
+                           D.data_ptr(), N, tcg.OUT_F32, 1.0, -2.0,
+                           torch.cuda.current_stream().cuda_stream)
+    assert st == tcg.OK
+    torch.cuda.synchronize()
+    assert torch.equal(D, -2.0 * C)
+
+
+# ------------------------------------------------------------ FP8 per tensor
+
+FP8_SHAPES = [(1, 16, 32), (128, 256, 128), (200, 300, 1000), (513, 700, 384),
+              (256, 1024, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", FP8_SHAPES)
+@pytest.mark.parametrize("out,beta", [("f32", 0.0), ("bf16", 0.0), ("bf16", 1.0)])
+def test_fp8_tensor_shapes(M, N, K, out, beta):
+    w = fp8_case(M, N, K, seed=M + N + K, mode="tensor", out=out, beta=beta)
+    check_full(w, run(w))
+
+
+def test_fp8_tensor_scales_bit_exact():
+    """Small-integer E4M3 codes with power-of-two scales: D is exact in FP32."""
+    M, N, K = 150, 270, 512
+    rng = np.random.default_rng(5)
+    ints = np.array([-4, -3, -2, -1, 0, 1, 2, 3, 4], np.float32)
+    w = W.Workload("fp8_exact", M, N, K, "fp8_tensor", "f32", alpha=1.0)
+    w.A = synth.to_e4m3(rng.choice(ints, size=(M, K)))
+    w.B = synth.to_e4m3(rng.choice(ints, size=(N, K)))
+    w.a_scale = np.array([2.0 ** -3], np.float32)
+    w.b_scale = np.array([2.0 ** 5], np.float32)
+    v, _ = oracle_for(w)
+    assert np.array_equal(d_to_host(run(w)).astype(np.float64), v)
+
+
+# ------------------------------------------------------- FP8 block, skinny M
+
+SKINNY = [(1, 128, 128), (16, 300, 200), (17, 1024, 4096), (64, 2000, 1000),
+          (100, 1024, 4096), (128, 256, 8192), (128, 4096, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SKINNY)
+@pytest.mark.parametrize("out,beta", [("f32", 0.0), ("bf16", 0.0), ("bf16", -1.0)])
+def test_fp8_block_skinny_shapes(M, N, K, out, beta):
+    w = fp8_case(M, N, K, seed=3 * M + N + K, mode="block", out=out, beta=beta, outliers=0.01)
+    check_full(w, run(w))
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 260, 300), (64, 1024, 4096), (128, 2048, 2048)])
+def test_fp8_block_scale_indexing_bit_exact(M, N, K):
+    """Power-of-two block scales that depend on (row, K block) and (N block,
+    K block) with small-integer codes: every misplaced scale changes bits."""
+    KB, NB = (K + 127) // 128, (N + 127) // 128
+    rng = np.random.default_rng(M + N)
+    ints = np.array([-3, -2, -1, 0, 1, 2, 3], np.float32)
+    w = W.Workload("fp8_block_exact", M, N, K, "fp8_block", "f32")
+    ldk = _pad(K, 16)
+    a = np.zeros((M, ldk), np.float32)
+    b = np.zeros((N, ldk), np.float32)
+    a[:, :K] = rng.choice(ints, size=(M, K))
+    b[:, :K] = rng.choice(ints, size=(N, K))
+    w.A, w.B = synth.to_e4m3(a), synth.to_e4m3(b)
+    w.a_scale = np.array([2.0 ** ((i % 3) - 1 + (kb % 2)) for kb in range(KB) for i in range(M)],
+                         np.float32)
+    w.b_scale = np.array([2.0 ** ((nb + kb) % 2) for nb in range(NB) for kb in range(KB)],
+                         np.float32)
+    v, _ = oracle_for(w)
+    assert np.array_equal(d_to_host(run(w)).astype(np.float64), v)
+
+
+def test_fp8_block_skinny_deterministic():
+    w = fp8_case(64, 4096, 4096, seed=11, mode="block", out="f32", outliers=0.01)
+    d1 = d_to_host(run(w))
+    d2 = d_to_host(run(w))
+    assert np.array_equal(d1.view(np.uint32), d2.view(np.uint32))
+
+
+# ------------------------------------------------------------ full workloads
+
+def _sampled(w, out, ntiles=16):
+    D = run(w, out=out)
+    tiles = sample_tiles(w.M, w.N, n=ntiles)
+    vs, bs = oracle_for(w, tiles=tiles)
+    got = d_to_host(D)
+    kind = "bf16" if w.kind == "bf16" else "fp8"
+    worst = 0.0
+    for (i0, j0, mi, nj), v, b in zip(tiles, vs, bs):
+        g = got[i0:i0 + mi, j0:j0 + nj]
+        c = c_values(w.C[i0:i0 + mi, j0:j0 + nj]) if w.C is not None else None
+        if g.dtype == np.uint16:
+            worst = max(worst, check_bf16(kind, g, v, b, w.beta, c, what=f"{w.name} {i0},{j0}"))
+        else:
+            worst = max(worst, check_f32(kind, g, v, b, w.beta, c, what=f"{w.name} {i0},{j0}"))
+    del D
+    torch.cuda.empty_cache()
+    return worst
+
+
+@pytest.mark.parametrize("name", ["bf16_4096", "fp8_4096", "bf16_mlp"])
+def test_full_size_sampled(name):
+    w = W.make(name)
+    _sampled(w, out="f32")   # pre-cast check with the same kernel
+    _sampled(w, out=w.out)   # the workload's own output type
+
+
+@pytest.mark.parametrize("M", [16, 64, 128])
+def test_skinny_full_size_sampled(M):
+    w = W.make(f"fp8_skinny_{M}")
+    for out in ("f32", "bf16"):
+        D = run(w, out=out)
+        tiles = [(0, j0, M, 128) for j0 in (0, 128, 4096, 8064)] + [
+            (0, int(j), M, 128) for j in np.random.default_rng(M).integers(0, 63, 4) * 128]
+        vs, bs = oracle_for(w, tiles=tiles)
+        got = d_to_host(D)
+        for (i0, j0, mi, nj), v, b in zip(tiles, vs, bs):
+            g = got[i0:i0 + mi, j0:j0 + nj]
+            if out == "f32":
+                check_f32("fp8", g, v, b, what=f"{w.name} {j0}")
+            else:
+                check_bf16("fp8", g, v, b, what=f"{w.name} {j0}")
+
+
+def test_launch_counter_and_status():
+    import tensor_core_dense_gb300 as tcg
+    n0 = tcg.launch_count()
+    w = bf16_case(64, 64, 64, seed=1)
+    run(w)
+    torch.cuda.synchronize()
+    assert tcg.launch_count() == n0 + 1
+    assert tcg.last_device_status() == tcg.OK
