@@ -1,0 +1,458 @@
+"""Benchmark: dense tensor-core GEMM on one GB300 (BF16 and FP8 E4M3).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one call of the library on the headline workload, the BF16
+4096 x 4096 x 4096 GEMM (A, B ~ N(0,1) rounded to BF16, BF16 output), the
+square problem of "Tensor Cores: Matrix Instructions, Swizzling and FP8,
+Measured" (Step 2).  The inputs (67 MB) fit in the 129 MB L2, so L2 is
+flushed (a 512 MiB write) before every timed step, outside the step's CUDA
+events.  The metric is TFLOPS = 2*M*N*K / time.
+
+Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs its own
+replica of the workload (GEMMs shard without any exchange; "replicas only"),
+times are maxed over ranks, and value = all ranks' FLOPs / that time.
+
+--impl reference times the CPU oracle (the plain FP64 reference of the same
+GEMM) on the host cores, on a bounded sample of output tiles per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 512 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def kernel_source_sha():
+    """sha256 over the CUDA sources, to tell whether a stored ncu figure is current."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_core_dense_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def stored_traffic(summary="gemm_tn_bf16_4096.md"):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is missing or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith(("source_sha256", "traffic_bytes")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("source_sha256") != kernel_source_sha():
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("hbm_gbs", 6800.0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every `ms` milliseconds."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str, ms: int = 50):
+        self.proc = None
+        self.t0 = time.time()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", device_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), max=float(f[2]),
+                                 power=float(f[3]) if f[3] not in ("[N/A]", "") else 0.0,
+                                 hw=f[5], hw_thermal=f[6], sw_thermal=f[7], sw_power=f[8]))
+            except ValueError:
+                continue
+        return rows
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                            ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# -------------------------------------------------------------- our path
+
+def _dist_init(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def _barrier_max(value, world):
+    """Max of a float over ranks (and a barrier)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def device_tensors(w):
+    import numpy as np
+    import torch
+    A = torch.from_numpy(w.A.view(np.int16)).cuda().view(torch.bfloat16) if w.kind == "bf16" \
+        else torch.from_numpy(w.A).cuda()
+    B = torch.from_numpy(w.B.view(np.int16)).cuda().view(torch.bfloat16) if w.kind == "bf16" \
+        else torch.from_numpy(w.B).cuda()
+    return A, B
+
+
+def make_call(w, A, B, D, C=None, sa=None, sb=None):
+    """A zero-argument closure that enqueues the library call on the current stream."""
+    import torch
+
+    import tensor_core_dense_gb300 as tcg
+    if w.kind == "bf16":
+        def call():
+            tcg.gemm_bf16(A, B, D, C, alpha=w.alpha, beta=w.beta,
+                          stream=torch.cuda.current_stream())
+    else:
+        mode = tcg.SCALE_TENSOR if w.kind == "fp8_tensor" else tcg.SCALE_BLOCK128
+
+        def call():
+            tcg.gemm_fp8_e4m3(A, B, sa, sb, D, C, mode=mode, alpha=w.alpha, beta=w.beta,
+                              stream=torch.cuda.current_stream())
+    return call
+
+
+def time_steps(call, steps, warmup, flush_buf):
+    """Per-step CUDA-event durations (ms) of `call`, L2 flushed before each step."""
+    import torch
+    for _ in range(warmup):
+        flush_buf.fill_(1.0)
+        call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush_buf.fill_(float(i))
+        starts[i].record()
+        call()
+        ends[i].record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def secondary_configs(flush_buf, steps=20, warmup=3):
+    """The other workloads, timed the same way (context beside the main line)."""
+    import torch
+
+    import synth.workloads as W
+    out = []
+    for name in ("fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64", "fp8_skinny_128"):
+        w = W.make(name)
+        A, B = device_tensors(w)
+        D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+        C = None
+        if w.C is not None:
+            import numpy as np
+            C = torch.from_numpy(w.C.view(np.int16)).cuda().view(torch.bfloat16)
+        sa = torch.from_numpy(w.a_scale).cuda() if w.a_scale is not None else None
+        sb = torch.from_numpy(w.b_scale).cuda() if w.b_scale is not None else None
+        ms = statistics.median(time_steps(make_call(w, A, B, D, C, sa, sb), steps, warmup,
+                                          flush_buf))
+        nbytes = w.A.nbytes + w.B.nbytes + D.numel() * 2 + (w.C.nbytes if w.C is not None else 0)
+        nbytes += (w.a_scale.nbytes if w.a_scale is not None else 0) + (
+            w.b_scale.nbytes if w.b_scale is not None else 0)
+        out.append({"workload": name, "M": w.M, "N": w.N, "K": w.K,
+                    "tflops": round(w.flops / (ms * 1e-3) / 1e12, 1),
+                    "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "ms": round(ms, 4)})
+        del A, B, D, C
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline_sample(w, seconds=12.0):
+    """The oracle as it stands, on seeded 128 x 128 output tiles of the workload,
+    until about `seconds` of wall time; TFLOPS of FP64 reference work."""
+    import numpy as np
+
+    import oracle
+    cores = oracle.default_threads()
+    rng = np.random.default_rng(0)
+    done_flops, t_used, ntiles = 0, 0.0, 0
+    batch = max(cores, 8)
+    while t_used < seconds:
+        tiles = [(int(rng.integers(0, w.M // 128)) * 128, int(rng.integers(0, w.N // 128)) * 128,
+                  128, 128) for _ in range(batch)]
+        t0 = time.perf_counter()
+        oracle.gemm(w.M, w.N, w.K, w.A, w.lda, w.B, w.ldb, tiles=tiles, nthreads=cores)
+        t_used += time.perf_counter() - t0
+        done_flops += batch * 2 * 128 * 128 * w.K
+        ntiles += batch
+    return {"value": round(done_flops / t_used / 1e12, 6), "unit": "TFLOPS", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{ntiles} output tiles of 128x128 (K={w.K}) of the {w.M}x{w.N}x{w.K} "
+                      f"BF16 GEMM, FP64, {t_used:.1f} s"}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import synth.workloads as W
+    import tensor_core_dense_gb300 as tcg
+
+    world, rank, local = _dist_init(args)
+    torch.cuda.set_device(local)
+    tcg.lib()
+    w = W.make("bf16_4096")
+    A, B = device_tensors(w)
+    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    call = make_call(w, A, B, D)
+
+    dev_uuid = str(torch.cuda.get_device_properties(local).uuid)
+    smi_id = dev_uuid if dev_uuid.startswith("GPU-") else f"GPU-{dev_uuid}"
+    sampler = ClockSampler(smi_id)
+
+    # warm-up, then the timed region: barrier + synchronize on both sides
+    for _ in range(args.warmup):
+        flush_buf.fill_(1.0)
+        call()
+    torch.cuda.synchronize()
+    _barrier(world)
+    n0 = tcg.launch_count()
+    times = time_steps(call, args.steps, 0, flush_buf)
+    launches = tcg.launch_count() - n0
+    torch.cuda.synchronize()
+    _barrier(world)
+    clocks = ClockSampler.summary(sampler.stop())
+    assert tcg.last_device_status() == tcg.OK
+
+    total_ms = _barrier_max(sum(times), world)
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: H2D of A and B from
+    # pinned memory, the GEMM, D2H of D, every step
+    ha = torch.from_numpy(w.A.view(np.int16)).pin_memory()
+    hb = torch.from_numpy(w.B.view(np.int16)).pin_memory()
+    hd = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
+    Ai, Bi = A.view(torch.int16), B.view(torch.int16)
+    e2e_steps = min(args.steps, 50)
+
+    def e2e_step():
+        Ai.copy_(ha, non_blocking=True)
+        Bi.copy_(hb, non_blocking=True)
+        call()
+        hd.copy_(D.view(torch.int16), non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = _barrier_max(e0.elapsed_time(e1), world)
+    e2e_value = world * w.flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    peak_bf16, _, peak_src = peaks()
+    per_launch_ms = statistics.mean(times)
+    achieved = w.flops / (per_launch_ms * 1e-3) / 1e12
+    line = {
+        "metric": "GEMM TFLOPS (BF16, FP8 E4M3) on 1 GB300; % of dense tensor-core peak",
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "bf16_4096: BF16 GEMM M=N=K=4096, A,B ~ N(0,1) rounded to BF16, "
+                               "BF16 output, alpha=1, beta=0",
+                   "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every timed step (512 MiB write outside the events)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peak_bf16, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_bf16, 4),
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "kernel": "gemm_tn_kernel<bf16,bf16 out>",
+                     "traffic": stored_traffic() if args.traffic is None else args.traffic},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS",
+                "h2d_bytes_per_step": int(w.A.nbytes + w.B.nbytes),
+                "d2h_bytes_per_step": int(D.numel() * 2)},
+    }
+    if rank == 0 and not args.no_secondary:
+        line["other_configs"] = secondary_configs(flush_buf)
+        for o in line["other_configs"]:
+            if o["workload"].startswith("fp8"):
+                o["frac_of_fp8_peak"] = round(o["tflops"] / (peak_bf16 * FP8_OVER_BF16), 4)
+            else:
+                o["frac_of_bf16_peak"] = round(o["tflops"] / peak_bf16, 4)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference
+
+def run_reference(args):
+    """The CPU oracle as it stands, on rank 0, one bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import synth.workloads as W
+    w = W.make("bf16_4096")
+    cores = oracle.default_threads()
+    rng = np.random.default_rng(1)
+
+    def tiles(n, size):
+        return [(int(rng.integers(0, w.M // size)) * size, int(rng.integers(0, w.N // size)) * size,
+                 size, size) for _ in range(n)]
+
+    # size each step so the whole run stays within about two minutes
+    t0 = time.perf_counter()
+    oracle.gemm(w.M, w.N, w.K, w.A, w.lda, w.B, w.ldb, tiles=tiles(cores, 32), nthreads=cores)
+    t_tile = max(time.perf_counter() - t0, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    per_step = max(1, int(budget / t_tile)) * cores
+    step_flops = per_step * 2 * 32 * 32 * w.K
+    for _ in range(args.warmup):
+        oracle.gemm(w.M, w.N, w.K, w.A, w.lda, w.B, w.ldb, tiles=tiles(per_step, 32),
+                    nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(w.M, w.N, w.K, w.A, w.lda, w.B, w.ldb, tiles=tiles(per_step, 32),
+                    nthreads=cores)
+    dt = time.perf_counter() - t0
+    value = step_flops * args.steps / dt / 1e12
+    sample = (f"{per_step} output tiles of 32x32 (K={w.K}) per step of the 4096^3 BF16 GEMM, "
+              f"FP64 oracle")
+    line = {
+        "impl": "reference",
+        "metric": "GEMM TFLOPS (BF16, FP8 E4M3) on 1 GB300; % of dense tensor-core peak",
+        "value": round(value, 6), "unit": "TFLOPS", "n_gpus": int(os.environ.get("WORLD_SIZE", 1)),
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "bf16_4096: BF16 GEMM M=N=K=4096, A,B ~ N(0,1) rounded to BF16, "
+                               "BF16 output, alpha=1, beta=0",
+                   "M": w.M, "N": w.N, "K": w.K},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the timed kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
