@@ -107,6 +107,38 @@ tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t
                          tcg_scale_mode mode, const void* C, int64_t ldc, void* D, int64_t ldd,
                          tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream);
 
+/*
+ * gemm_fp8_e4m3_block_noalloc -- the TCG_SCALE_BLOCK128 case of gemm_fp8_e4m3
+ * (M <= 128) without any device allocation.  The pages have no counterpart
+ * to this entry point; it exists for callers that cannot let a library call
+ * cudaMalloc: code being recorded into a CUDA graph (an allocation during
+ * stream capture breaks the capture), latency-bound loops that cannot absorb
+ * the device-wide synchronisation cudaMalloc/cudaFree can imply, and programs
+ * whose own memory manager owns all of device memory.
+ *
+ * Arguments, layouts, alignment and numerics are those of gemm_fp8_e4m3 with
+ * mode = TCG_SCALE_BLOCK128.  The split-K scratch is a fixed 32 MiB array
+ * inside the library's device code, present on every device that loads the
+ * library until the process exits; the caller still provides A, B, the
+ * scales, C and D.  A problem whose scratch would exceed 32 MiB (counters:
+ * ceil(N/128) words rounded up to 256 bytes; partial sums: ceil(N/128) x
+ * segments-per-tile x Mp x 128 FP32 values, Mp = M rounded up to 16/32/64/128)
+ * is rejected with TCG_ERR_UNSUPPORTED before anything is enqueued; M > 128
+ * is rejected the same way.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and raises the kernel's shared-memory limit; make that
+ * first call before any stream capture.  Each call clears the tile counters
+ * (a memset on `stream`) and then launches one kernel.  All calls on a device
+ * share the one array: calls whose executions overlap on the GPU (different
+ * streams without ordering between them) race on it and give wrong results.
+ */
+tcg_status gemm_fp8_e4m3_block_noalloc(int64_t M, int64_t N, int64_t K, const void* A,
+                                       int64_t lda, const void* B, int64_t ldb,
+                                       const float* a_scale, const float* b_scale, const void* C,
+                                       int64_t ldc, void* D, int64_t ldd, tcg_out_dtype out_dtype,
+                                       float alpha, float beta, tcg_stream stream);
+
 /* A static, human-readable name for a status code. */
 const char* tcg_status_string(tcg_status status);
 

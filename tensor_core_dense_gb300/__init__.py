@@ -23,8 +23,8 @@ OUT_BF16, OUT_F32 = 0, 1
 SCALE_TENSOR, SCALE_BLOCK128 = 0, 1
 
 # Every symbol include/tcgemm.h declares.
-EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "tcg_status_string", "tcg_last_device_status",
-           "tcg_launch_count")
+EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8_e4m3_block_noalloc", "tcg_status_string",
+           "tcg_last_device_status", "tcg_launch_count")
 
 _lib = None
 

@@ -416,3 +416,142 @@ tcg_status tcg_last_device_status(tcg_stream stream) {
 uint64_t tcg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Allocation-free variant of the block-scaled skinny FP8 path.
+//
+// gemm_fp8_e4m3 allocates its split-K workspace with cudaMalloc on first use
+// (and again, after a device-wide synchronisation, whenever a larger one is
+// needed).  Some callers cannot allow that: code that records CUDA graphs
+// (an allocation inside stream capture invalidates the capture), serving
+// loops that must never stall on the implicit synchronisation of
+// cudaMalloc/cudaFree, and applications whose memory manager owns all of
+// device memory and forbids allocations behind its back.  For them,
+// gemm_fp8_e4m3_block_noalloc runs the same kernel with its scratch in a
+// fixed array that is part of the loaded module.
+namespace tcg {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per device
+
+// Scratch for the allocation-free entry point: tile counters first (zeroed by
+// every call), then the FP32 partial-sum slots.  Every device that loads this
+// library holds it until the process exits.  In host code this name is only a
+// stand-in for the symbol; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) and cached.
+tcg_status noalloc_scratch(int dev, void** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return TCG_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TCG_OK;
+}
+
+// Encodes a tensor map on the stack (the cached path would insert into a
+// host-side table, which allocates).
+tcg_status encode_map_uncached(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t rows,
+                               uint64_t ld_bytes, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return TCG_ERR_CUDA;
+  std::memset(out, 0, sizeof *out);
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {ld_bytes};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? TCG_OK
+             : TCG_ERR_CUDA;
+}
+
+template <int kMp>
+tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* sb,
+                                 cudaStream_t stream, int dev, int sms) {
+  using Cfg = SkinnyCfg<kMp>;
+  SkinnyParams p{};
+  p.M = (int32_t)a.M;
+  p.N = (int32_t)a.N;
+  p.K = (int32_t)a.K;
+  p.n_tiles = (int32_t)((a.N + 127) / 128);
+  p.num_kb = (int32_t)((a.K + 127) / 128);
+  const int64_t T = (int64_t)p.n_tiles * p.num_kb;
+  if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
+  p.total_steps = (int32_t)T;
+  p.grid = (int32_t)(T < sms ? T : sms);
+  const int64_t min_range = T / p.grid;
+  p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);
+  if (p.max_seg > p.grid) p.max_seg = p.grid;
+  const size_t counter_bytes = ((size_t)p.n_tiles * sizeof(unsigned int) + 255) & ~size_t(255);
+  const size_t partial_bytes = (size_t)p.n_tiles * p.max_seg * kMp * 128 * sizeof(float);
+  if (counter_bytes + partial_bytes > kNoAllocScratchBytes) return TCG_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (tcg_status s = noalloc_scratch(dev, &scratch); s != TCG_OK) return s;
+  p.counters = static_cast<unsigned int*>(scratch);
+  p.ws = reinterpret_cast<float*>(static_cast<char*>(scratch) + counter_bytes);
+  // The array keeps whatever the previous call left; the counters must
+  // start at zero.
+  if (cudaMemsetAsync(scratch, 0, counter_bytes, stream) != cudaSuccess) return TCG_ERR_CUDA;
+  CUtensorMap ma, mb;
+  if (tcg_status s = encode_map_uncached(&ma, a.A, a.K, a.M, a.lda, kMp); s != TCG_OK) return s;
+  if (tcg_status s = encode_map_uncached(&mb, a.B, a.K, a.N, a.ldb, 128); s != TCG_OK) return s;
+  p.a_scale = sa;
+  p.b_scale = sb;
+  p.C = a.beta != 0.0f ? a.C : nullptr;
+  p.ldc = a.ldc;
+  p.D = a.D;
+  p.ldd = a.ldd;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.out_f32 = a.out == TCG_OUT_F32;
+  p.has_c = a.beta != 0.0f;
+  auto* fn = &gemm_fp8_block_skinny_kernel<kMp>;
+  {  // raise the shared-memory limit once per device (no host-side table)
+    static bool raised[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!raised[dev]) {
+      if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Cfg::kSmemBytes) != cudaSuccess)
+        return TCG_ERR_CUDA;
+      raised[dev] = true;
+    }
+  }
+  fn<<<p.grid, kSkThreads, Cfg::kSmemBytes, stream>>>(ma, mb, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tcg
+
+extern "C" tcg_status gemm_fp8_e4m3_block_noalloc(int64_t M, int64_t N, int64_t K, const void* A,
+                                                  int64_t lda, const void* B, int64_t ldb,
+                                                  const float* a_scale, const float* b_scale,
+                                                  const void* C, int64_t ldc, void* D,
+                                                  int64_t ldd, tcg_out_dtype out_dtype,
+                                                  float alpha, float beta, tcg_stream stream) {
+  const Common a{M, N, K, A, B, C, lda, ldb, ldc, ldd, D, (int)out_dtype, alpha, beta};
+  if (tcg_status s = validate(a, 1); s != TCG_OK) return s;
+  if (M == 0 || N == 0) return TCG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_k0(a, st);
+  if (!a_scale || !b_scale) return TCG_ERR_INVALID_ARG;
+  if (M > 128) return TCG_ERR_UNSUPPORTED;
+  int dev, sms;
+  if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+  if (M <= 16) return launch_skinny_noalloc<16>(a, a_scale, b_scale, st, dev, sms);
+  if (M <= 32) return launch_skinny_noalloc<32>(a, a_scale, b_scale, st, dev, sms);
+  if (M <= 64) return launch_skinny_noalloc<64>(a, a_scale, b_scale, st, dev, sms);
+  return launch_skinny_noalloc<128>(a, a_scale, b_scale, st, dev, sms);
+}
