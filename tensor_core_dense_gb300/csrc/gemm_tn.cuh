@@ -7,8 +7,14 @@
 // FP8 E4M3 (kind::f8f6f4); accumulation is FP32 in Tensor Memory.
 //
 // One CTA per SM loops over 128 x 256 output tiles (persistent scheduler,
-// grouped raster for L2 reuse).  Its six warps have fixed roles:
-//
+// grouped raster for L2 reuse).  Whole waves of tiles run one tile per CTA.
+// The tiles of a last, partial wave (or of a grid smaller than the GPU) are
+// cut along N into 2 or 4 sub-tiles of 128 or 64 columns (UMMA N = 128 / 64)
+// so that the last wave keeps every SM busy for a half or a quarter of a tile
+// time instead of leaving most SMs idle for a whole one.  Each output element
+// is still produced by exactly one CTA from all of K: no workspace, no
+// reduction, bit-identical results from run to run.  Its six warps have fixed
+// roles:
 //   warp 0     one lane issues TMA loads of 128-byte-swizzled A/B K-blocks
 //              into a kStages-deep ring of shared-memory stages, each stage
 //              guarded by a `full` mbarrier (TMA transaction bytes) and an
@@ -54,6 +60,7 @@ constexpr uint32_t kATileBytes = kBM * kBKBytes;
 constexpr uint32_t kBTileBytes = kBN * kBKBytes;
 constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kNumBars = 2 * kStages + 5;  // full, empty, tmem_full x2, tmem_empty x2, drain
+constexpr int kBBoxRows = 64;              // B is loaded as 64-row boxes (1, 2 or 4 per stage)
 constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align*/;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kGroupM = 16;            // raster: tile-rows per group
@@ -65,7 +72,11 @@ __device__ unsigned int g_tcg_status = 0;
 struct GemmParams {
   int32_t M, N, K;
   int32_t tiles_m, tiles_n, num_kb, num_tiles;
-  int32_t pad_;
+  // schedule: CTA b takes whole tiles b + i*gridDim.x (i < dp_waves, tile <
+  // dp_end), then sub-tile units u = b + j*gridDim.x (u < (num_tiles -
+  // dp_end) * split) of the remaining tiles, each split into `split` pieces
+  // along N.
+  int32_t dp_waves, dp_end, split, pad_;
   const void* C;
   int64_t ldc;
   void* D;
@@ -111,6 +122,122 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = local / gm;
 }
 
+// One unit of work: columns [sub*256/split, (sub+1)*256/split) of tile `tile`.
+struct WorkItem {
+  int tile, sub, split;
+};
+
+// The sequence of work items of one CTA; every role walks the same sequence.
+struct WorkIter {
+  int b, G, i, j, dp_waves, dp_end, split, tail_units;
+  __device__ __forceinline__ void init(const GemmParams& p) {
+    b = blockIdx.x;
+    G = gridDim.x;
+    i = j = 0;
+    dp_waves = p.dp_waves;
+    dp_end = p.dp_end;
+    split = p.split;
+    tail_units = (p.num_tiles - p.dp_end) * p.split;
+  }
+  __device__ __forceinline__ bool next(WorkItem& w) {
+    while (i < dp_waves) {
+      const int t = b + i * G;
+      ++i;
+      if (t < dp_end) {
+        w.tile = t;
+        w.sub = 0;
+        w.split = 1;
+        return true;
+      }
+    }
+    const int u = b + j * G;
+    if (u < tail_units) {
+      ++j;
+      w.tile = dp_end + u / split;
+      w.sub = u % split;
+      w.split = split;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Scales 32 accumulator values of one row, adds beta*C, converts and stores
+// them at D[row, col0 .. col0+31] (columns >= N are skipped).
+template <int kOut, bool kHasC>
+__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int row, int col0,
+                                                const float (&acc)[32], float scale) {
+  if (row >= p.M || col0 >= p.N) return;
+  const bool full_chunk = col0 + 32 <= p.N;
+  const float beta = p.beta;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = scale * acc[j];
+  if (kOut == 1) {
+    float* drow = static_cast<float*>(p.D) + (int64_t)row * p.ldd + col0;
+    const float* crow =
+        kHasC ? static_cast<const float*>(p.C) + (int64_t)row * p.ldc + col0 : nullptr;
+    if (full_chunk) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        if (kHasC) {
+          const float4 cv = *reinterpret_cast<const float4*>(crow + j);
+          o.x += beta * cv.x;
+          o.y += beta * cv.y;
+          o.z += beta * cv.z;
+          o.w += beta * cv.w;
+        }
+        *reinterpret_cast<float4*>(drow + j) = o;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (col0 + j < p.N) {
+          float o = v[j];
+          if (kHasC) o += beta * crow[j];
+          drow[j] = o;
+        }
+      }
+    }
+  } else {
+    uint16_t* drow = static_cast<uint16_t*>(p.D) + (int64_t)row * p.ldd + col0;
+    const uint16_t* crow =
+        kHasC ? static_cast<const uint16_t*>(p.C) + (int64_t)row * p.ldc + col0 : nullptr;
+    if (full_chunk) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        if (kHasC) {
+          const uint4 cv = *reinterpret_cast<const uint4*>(crow + j);
+          v[j + 0] += beta * bf16_lo_to_f32(cv.x);
+          v[j + 1] += beta * bf16_hi_to_f32(cv.x);
+          v[j + 2] += beta * bf16_lo_to_f32(cv.y);
+          v[j + 3] += beta * bf16_hi_to_f32(cv.y);
+          v[j + 4] += beta * bf16_lo_to_f32(cv.z);
+          v[j + 5] += beta * bf16_hi_to_f32(cv.z);
+          v[j + 6] += beta * bf16_lo_to_f32(cv.w);
+          v[j + 7] += beta * bf16_hi_to_f32(cv.w);
+        }
+        uint4 o;
+        o.x = pack_bf16x2(v[j + 0], v[j + 1]);
+        o.y = pack_bf16x2(v[j + 2], v[j + 3]);
+        o.z = pack_bf16x2(v[j + 4], v[j + 5]);
+        o.w = pack_bf16x2(v[j + 6], v[j + 7]);
+        *reinterpret_cast<uint4*>(drow + j) = o;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (col0 + j < p.N) {
+          float o = v[j];
+          if (kHasC) o += beta * __uint_as_float((uint32_t)crow[j] << 16);
+          drow[j] = (uint16_t)(pack_bf16x2(o, 0.0f) & 0xFFFFu);
+        }
+      }
+    }
+  }
+}
+
 // kIn: 0 = BF16, 1 = E4M3.  kOut: 0 = BF16, 1 = FP32.  kHasC: beta != 0.
 template <int kIn, int kOut, bool kHasC>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -118,7 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   constexpr int kBKElems = kIn == 0 ? kBKBytes / 2 : kBKBytes;
   // BF16 -> format 1 of kind::f16; E4M3 -> format 0 of kind::f8f6f4.
-  constexpr uint32_t kIdesc = kIn == 0 ? make_idesc(1, 1, kBM, kBN) : make_idesc(0, 0, kBM, kBN);
+  constexpr uint32_t kFmt = kIn == 0 ? 1u : 0u;
+  constexpr uint32_t kIdesc256 = make_idesc(kFmt, kFmt, kBM, 256);
+  constexpr uint32_t kIdesc128 = make_idesc(kFmt, kFmt, kBM, 128);
+  constexpr uint32_t kIdesc64 = make_idesc(kFmt, kFmt, kBM, 64);
   // Each MMA consumes 32 bytes of K (16 BF16 or 32 E4M3 values); the
   // descriptor start address advances by 32 bytes (2 in its >>4 units)
   // inside the 128-byte swizzled row.
@@ -173,18 +303,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmap_b);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      WorkIter wi;
+      wi.init(p);
+      WorkItem w;
+      while (ok && wi.next(w)) {
         int tm, tn;
-        tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
+        tile_coords(w.tile, p.tiles_m, p.tiles_n, tm, tn);
+        const int nboxes = (kBN / kBBoxRows) / w.split;
+        const int brow0 = tn * kBN + w.sub * (kBN / w.split);
+        const uint32_t bytes = kATileBytes + (uint32_t)nboxes * kBBoxRows * kBKBytes;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
           if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, 1)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+          mbar_arrive_expect_tx(full_bar(s), bytes);
           tma_load_2d(a_smem(s), &tmap_a, full_bar(s), kb * kBKElems, tm * kBM);
-          tma_load_2d(b_smem(s), &tmap_b, full_bar(s), kb * kBKElems, tn * kBN);
+          for (int bx = 0; bx < nboxes; ++bx)
+            tma_load_2d(b_smem(s) + (uint32_t)bx * kBBoxRows * kBKBytes, &tmap_b, full_bar(s),
+                        kb * kBKElems, brow0 + bx * kBBoxRows);
         }
       }
       if (!ok) {
@@ -203,11 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, lt = 0;
       bool ok = true, issued = false;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++lt) {
+      WorkIter wi;
+      wi.init(p);
+      WorkItem w;
+      for (; ok && wi.next(w); ++lt) {
         const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
         if (!wait_phase(tempty_bar(acc), aph ^ 1u, abort_flag, 2)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
+        const uint32_t idesc = w.split == 1 ? kIdesc256 : w.split == 2 ? kIdesc128 : kIdesc64;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
           if (!wait_phase(full_bar(s), ph, abort_flag, 3)) {
@@ -221,9 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kMmaPerStage; ++k) {
             const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
             if (kIn == 0)
-              mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, accumulate);
+              mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, idesc, accumulate);
             else
-              mma_e4m3(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, accumulate);
+              mma_e4m3(d_tmem, ad + 2u * k, bd + 2u * k, idesc, accumulate);
           }
           issued = true;
           tc_commit(empty_bar(s));
@@ -242,11 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------- epilogue
     const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may access
+    const int row_in_tile = (int)(q * 32u + lane);
     float scale = p.alpha;
     if (kIn == 1) scale = p.a_scale[0] * p.b_scale[0] * p.alpha;
-    const float beta = p.beta;
     uint32_t lt = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
+    WorkIter wi;
+    wi.init(p);
+    WorkItem w;
+    for (; wi.next(w); ++lt) {
       const uint32_t acc = lt & 1u, aph = (lt >> 1) & 1u;
       uint32_t ok = 0;
       if (lane == 0) ok = wait_phase(tfull_bar(acc), aph, abort_flag, 4) ? 1u : 0u;
@@ -254,90 +399,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after_sync();
       int tm, tn;
-      tile_coords(t, p.tiles_m, p.tiles_n, tm, tn);
-      const int row = tm * kBM + (int)(q * 32u + lane);
+      tile_coords(w.tile, p.tiles_m, p.tiles_n, tm, tn);
+      const int row = tm * kBM + row_in_tile;
+      const int col_base = tn * kBN + w.sub * (kBN / w.split);
+      const int nchunks = (kBN / 32) / w.split;
       const uint32_t t_row = tmem_base + ((q * 32u) << 16) + acc * kAccCols;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < nchunks; ++c) {
         uint32_t r[32];
         __syncwarp();  // tcgen05.ld is .sync.aligned: reconverge after the stores
         tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
         tmem_ld_wait(r);
-        if (c == kBN / 32 - 1) {
+        if (c == nchunks - 1) {
           // Accumulator fully read: hand the buffer back to the MMA warp.
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
-        const int col0 = tn * kBN + c * 32;
-        if (row >= p.M || col0 >= p.N) continue;
-        const bool full_chunk = col0 + 32 <= p.N;
-        float v[32];
+        float a[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = scale * __uint_as_float(r[j]);
-        if (kOut == 1) {
-          float* drow = static_cast<float*>(p.D) + (int64_t)row * p.ldd + col0;
-          const float* crow = kHasC ? static_cast<const float*>(p.C) + (int64_t)row * p.ldc + col0
-                                    : nullptr;
-          if (full_chunk) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-              if (kHasC) {
-                const float4 cv = *reinterpret_cast<const float4*>(crow + j);
-                o.x += beta * cv.x;
-                o.y += beta * cv.y;
-                o.z += beta * cv.z;
-                o.w += beta * cv.w;
-              }
-              *reinterpret_cast<float4*>(drow + j) = o;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < p.N) {
-                float o = v[j];
-                if (kHasC) o += beta * crow[j];
-                drow[j] = o;
-              }
-            }
-          }
-        } else {
-          uint16_t* drow = static_cast<uint16_t*>(p.D) + (int64_t)row * p.ldd + col0;
-          const uint16_t* crow =
-              kHasC ? static_cast<const uint16_t*>(p.C) + (int64_t)row * p.ldc + col0 : nullptr;
-          if (full_chunk) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              if (kHasC) {
-                const uint4 cv = *reinterpret_cast<const uint4*>(crow + j);
-                v[j + 0] += beta * bf16_lo_to_f32(cv.x);
-                v[j + 1] += beta * bf16_hi_to_f32(cv.x);
-                v[j + 2] += beta * bf16_lo_to_f32(cv.y);
-                v[j + 3] += beta * bf16_hi_to_f32(cv.y);
-                v[j + 4] += beta * bf16_lo_to_f32(cv.z);
-                v[j + 5] += beta * bf16_hi_to_f32(cv.z);
-                v[j + 6] += beta * bf16_lo_to_f32(cv.w);
-                v[j + 7] += beta * bf16_hi_to_f32(cv.w);
-              }
-              uint4 o;
-              o.x = pack_bf16x2(v[j + 0], v[j + 1]);
-              o.y = pack_bf16x2(v[j + 2], v[j + 3]);
-              o.z = pack_bf16x2(v[j + 4], v[j + 5]);
-              o.w = pack_bf16x2(v[j + 6], v[j + 7]);
-              *reinterpret_cast<uint4*>(drow + j) = o;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < p.N) {
-                float o = v[j];
-                if (kHasC) o += beta * __uint_as_float((uint32_t)crow[j] << 16);
-                drow[j] = (uint16_t)(pack_bf16x2(o, 0.0f) & 0xFFFFu);
-              }
-            }
-          }
-        }
+        for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
+        store_row_chunk<kOut, kHasC>(p, row, col_base + c * 32, a, scale);
       }
     }
   }

@@ -263,7 +263,8 @@ tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale
   CUtensorMap ma, mb;
   if (tcg_status s = tensor_map(&ma, dt, a.A, a.K, a.M, a.lda * in_bytes, box_k, kBM); s != TCG_OK)
     return s;
-  if (tcg_status s = tensor_map(&mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, box_k, kBN); s != TCG_OK)
+  if (tcg_status s = tensor_map(&mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, box_k, kBBoxRows);
+      s != TCG_OK)
     return s;
   GemmParams p{};
   p.M = (int32_t)a.M;
@@ -283,7 +284,27 @@ tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale
   p.beta = a.beta;
   p.a_scale = a_scale;
   p.b_scale = b_scale;
-  const int grid = (int)(tiles < sms ? tiles : sms);
+  // Schedule: whole waves of tiles run one tile per CTA; the tiles left for a
+  // last partial wave (or all tiles, when there are fewer than SMs) are cut
+  // along N into 2 or 4 sub-tiles when that still fits in one wave.
+  int grid;
+  int64_t rest;
+  if (tiles >= sms) {
+    grid = sms;
+    p.dp_waves = (int32_t)(tiles / sms);
+    rest = tiles % sms;
+  } else {
+    p.dp_waves = 0;
+    rest = tiles;
+  }
+  int split = 1;
+  if (rest > 0) {
+    if (rest * 4 <= sms) split = 4;
+    else if (rest * 2 <= sms) split = 2;
+  }
+  if (tiles < sms) grid = (int)(rest * split);
+  p.dp_end = (int32_t)(tiles - rest);
+  p.split = split;
   const bool has_c = a.beta != 0.0f;
   if (a.out == TCG_OUT_BF16)
     return has_c ? launch_tn_inst<kIn, 0, true>(ma, mb, p, grid, dev, stream)

@@ -101,6 +101,28 @@ def test_bf16_shapes(M, N, K, out, beta):
     check_full(w, run(w))
 
 
+# Shapes that take each branch of the scheduler on a 152-SM GB300: a partial
+# last wave cut into quarter tiles (160 tiles), half tiles (54 tiles), kept
+# whole (256 tiles: 104 left over), and small grids cut into quarters (BF16
+# and FP8).
+@pytest.mark.parametrize("M,N,K,kind", [(2048, 2560, 1024, "bf16"), (1100, 1300, 700, "bf16"),
+                                        (1000, 1000, 2048, "fp8"), (300, 600, 8192, "bf16"),
+                                        (4096, 2560, 512, "fp8"), (2048, 4096, 512, "bf16")])
+@pytest.mark.parametrize("out,beta", [("f32", 0.0), ("bf16", 1.0)])
+def test_tail_schedules(M, N, K, kind, out, beta):
+    if kind == "bf16":
+        w = bf16_case(M, N, K, seed=M + 2 * N + K, out=out, beta=beta)
+    else:
+        w = fp8_case(M, N, K, seed=M + 2 * N + K, mode="tensor", out=out, beta=beta)
+    check_full(w, run(w))
+
+
+def test_tail_schedule_deterministic():
+    w = bf16_case(1100, 1300, 4096, seed=4, out="f32")
+    d1, d2 = d_to_host(run(w)), d_to_host(run(w))
+    assert np.array_equal(d1.view(np.uint32), d2.view(np.uint32))
+
+
 def test_bf16_one_hot_indexing_bit_exact():
     """A has one 1 per row at column pi(i): the product is exactly B[j, pi(i)], so
     D[i, j] = fp32(alpha * B[j, pi(i)] + beta * C[i, j]) bit for bit (alpha, beta
