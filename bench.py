@@ -5,9 +5,11 @@
 A step is one call of the library on the headline workload, the BF16
 4096 x 4096 x 4096 GEMM (A, B ~ N(0,1) rounded to BF16, BF16 output), the
 square problem of "Tensor Cores: Matrix Instructions, Swizzling and FP8,
-Measured" (Step 2).  The inputs (67 MB) fit in the 129 MB L2, so L2 is
-flushed (a 512 MiB write) before every timed step, outside the step's CUDA
-events.  The metric is TFLOPS = 2*M*N*K / time.
+Measured" (Step 2).  One step's inputs (67 MB) would fit in the 129 MB L2, so
+the steps cycle through enough copies of the inputs (5) that every step reads
+operands that are not in L2.  The K timed steps run back to back from one
+CUDA graph, between one pair of CUDA events.  The metric is
+TFLOPS = 2*M*N*K / time.
 
 Rank 0 prints one JSON line.  With N > 1 (torchrun) every rank runs its own
 replica of the workload (GEMMs shard without any exchange; "replicas only"),
@@ -30,7 +32,6 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-L2_FLUSH_BYTES = 512 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0   # nominal dense ratio (4.5 / 2.25 PFLOP/s)
@@ -196,49 +197,110 @@ def make_call(w, A, B, D, C=None, sa=None, sb=None):
     return call
 
 
-def time_steps(call, steps, warmup, flush_buf):
-    """Per-step CUDA-event durations (ms) of `call`, L2 flushed before each step."""
+def l2_bytes():
     import torch
-    for _ in range(warmup):
-        flush_buf.fill_(1.0)
-        call()
-    torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for i in range(steps):
-        flush_buf.fill_(float(i))
-        starts[i].record()
-        call()
-        ends[i].record()
-    torch.cuda.synchronize()
-    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except (AttributeError, RuntimeError):
+        return 129 << 20
 
 
-def secondary_configs(flush_buf, steps=20, warmup=3):
+def rotation_count(input_bytes):
+    """Copies of the inputs to cycle through so no step finds its operands in
+    L2: enough that 2x the L2 size streams by between two uses of a copy."""
+    l2 = l2_bytes()
+    if input_bytes >= 2 * l2:
+        return 1
+    return -(-2 * l2 // max(1, input_bytes)) + 1
+
+
+class Rotation:
+    """R device copies of a workload's inputs and outputs, with one library
+    call closure per copy."""
+
+    def __init__(self, w, copies=None):
+        import numpy as np
+        import torch
+        inb = w.A.nbytes + w.B.nbytes + (w.C.nbytes if w.C is not None else 0)
+        self.input_bytes = inb
+        self.copies = copies or rotation_count(inb)
+        self.calls = []
+        self.tensors = []
+        for _ in range(self.copies):
+            A, B = device_tensors(w)
+            D = torch.empty((w.M, w.N), dtype=torch.bfloat16 if w.out == "bf16" else torch.float32,
+                            device="cuda")
+            C = None
+            if w.C is not None:
+                C = torch.from_numpy(w.C.view(np.int16)).cuda().view(torch.bfloat16)
+            sa = torch.from_numpy(w.a_scale).cuda() if w.a_scale is not None else None
+            sb = torch.from_numpy(w.b_scale).cuda() if w.b_scale is not None else None
+            self.tensors.append((A, B, C, D, sa, sb))
+            self.calls.append(make_call(w, A, B, D, C, sa, sb))
+
+    def step(self, i):
+        self.calls[i % self.copies]()
+
+    def describe(self):
+        mb = self.input_bytes / 1e6
+        if self.copies == 1:
+            return f"inputs larger than L2: {mb:.0f} MB per step (L2 {l2_bytes() / 1e6:.0f} MB)"
+        return (f"inputs larger than L2: {self.copies} copies of the {mb:.0f} MB inputs are "
+                f"cycled ({self.copies * mb:.0f} MB > L2 {l2_bytes() / 1e6:.0f} MB), so no step "
+                f"finds its operands in L2")
+
+
+def time_graph(rot, steps, warmup):
+    """Time `steps` back-to-back calls (cycling the copies) replayed from one
+    CUDA graph; returns (total ms, kernel launches inside the graph)."""
+    import torch
+
+    import tensor_core_dense_gb300 as tcg
+    for i in range(warmup):
+        rot.step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    n0 = tcg.launch_count()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(steps):
+            rot.step(i)
+    launches = tcg.launch_count() - n0
+    torch.cuda.synchronize()
+    g.replay()  # one untimed replay
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), launches, g
+
+
+SECONDARY = ("fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64", "fp8_skinny_128")
+
+
+def secondary_configs(steps=50, warmup=5, names=SECONDARY):
     """The other workloads, timed the same way (context beside the main line)."""
     import torch
 
     import synth.workloads as W
     out = []
-    for name in ("fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64", "fp8_skinny_128"):
+    for name in names:
         w = W.make(name)
-        A, B = device_tensors(w)
-        D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
-        C = None
-        if w.C is not None:
-            import numpy as np
-            C = torch.from_numpy(w.C.view(np.int16)).cuda().view(torch.bfloat16)
-        sa = torch.from_numpy(w.a_scale).cuda() if w.a_scale is not None else None
-        sb = torch.from_numpy(w.b_scale).cuda() if w.b_scale is not None else None
-        ms = statistics.median(time_steps(make_call(w, A, B, D, C, sa, sb), steps, warmup,
-                                          flush_buf))
-        nbytes = w.A.nbytes + w.B.nbytes + D.numel() * 2 + (w.C.nbytes if w.C is not None else 0)
+        rot = Rotation(w)
+        ms, _, g = time_graph(rot, steps, warmup)
+        ms /= steps
+        out_bytes = w.M * w.N * (2 if w.out == "bf16" else 4)
+        nbytes = rot.input_bytes + out_bytes
         nbytes += (w.a_scale.nbytes if w.a_scale is not None else 0) + (
             w.b_scale.nbytes if w.b_scale is not None else 0)
         out.append({"workload": name, "M": w.M, "N": w.N, "K": w.K,
                     "tflops": round(w.flops / (ms * 1e-3) / 1e12, 1),
-                    "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "ms": round(ms, 4)})
-        del A, B, D, C
+                    "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 2),
+                    "copies": rot.copies})
+        del rot, g
         torch.cuda.empty_cache()
     return out
 
@@ -278,35 +340,28 @@ def run_ours(args):
     torch.cuda.set_device(local)
     tcg.lib()
     w = W.make("bf16_4096")
-    A, B = device_tensors(w)
-    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
-    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    call = make_call(w, A, B, D)
+    rot = Rotation(w)
 
     dev_uuid = str(torch.cuda.get_device_properties(local).uuid)
     smi_id = dev_uuid if dev_uuid.startswith("GPU-") else f"GPU-{dev_uuid}"
     sampler = ClockSampler(smi_id)
-
-    # warm-up, then the timed region: barrier + synchronize on both sides
-    for _ in range(args.warmup):
-        flush_buf.fill_(1.0)
-        call()
-    torch.cuda.synchronize()
+    # W warm-up steps, capture of the K timed steps, then the timed replay
+    # (barrier + synchronize on both sides inside time_graph's sync points)
     _barrier(world)
-    n0 = tcg.launch_count()
-    times = time_steps(call, args.steps, 0, flush_buf)
-    launches = tcg.launch_count() - n0
-    torch.cuda.synchronize()
+    total_ms, launches, graph = time_graph(rot, args.steps, args.warmup)
     _barrier(world)
     clocks = ClockSampler.summary(sampler.stop())
     assert tcg.last_device_status() == tcg.OK
+    del graph
 
-    total_ms = _barrier_max(sum(times), world)
+    total_ms = _barrier_max(total_ms, world)
     ms_per_step = total_ms / args.steps
     value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
 
     # end to end through the public API with host buffers: H2D of A and B from
-    # pinned memory, the GEMM, D2H of D, every step
+    # pinned memory, the GEMM, D2H of D, every step (plain calls, no graph)
+    A, B, _, D, _, _ = rot.tensors[0]
+    call = rot.calls[0]
     ha = torch.from_numpy(w.A.view(np.int16)).pin_memory()
     hb = torch.from_numpy(w.B.view(np.int16)).pin_memory()
     hd = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
@@ -333,8 +388,7 @@ def run_ours(args):
     e2e_value = world * w.flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
     peak_bf16, _, peak_src = peaks()
-    per_launch_ms = statistics.mean(times)
-    achieved = w.flops / (per_launch_ms * 1e-3) / 1e12
+    achieved = w.flops / (ms_per_step * 1e-3) / 1e12
     line = {
         "metric": "GEMM TFLOPS (BF16, FP8 E4M3) on 1 GB300; % of dense tensor-core peak",
         "value": round(value, 2),
@@ -351,7 +405,9 @@ def run_ours(args):
         "config": {"workload": "bf16_4096: BF16 GEMM M=N=K=4096, A,B ~ N(0,1) rounded to BF16, "
                                "BF16 output, alpha=1, beta=0",
                    "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{world}",
-                   "l2": "flushed before every timed step (512 MiB write outside the events)"},
+                   "l2": rot.describe(),
+                   "timing": "K back-to-back library calls captured in one CUDA graph, one "
+                             "CUDA-event pair around its replay"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peak_bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_bf16, 4),
@@ -364,8 +420,10 @@ def run_ours(args):
                 "h2d_bytes_per_step": int(w.A.nbytes + w.B.nbytes),
                 "d2h_bytes_per_step": int(D.numel() * 2)},
     }
+    del rot, A, B, D
+    torch.cuda.empty_cache()
     if rank == 0 and not args.no_secondary:
-        line["other_configs"] = secondary_configs(flush_buf)
+        line["other_configs"] = secondary_configs()
         for o in line["other_configs"]:
             if o["workload"].startswith("fp8"):
                 o["frac_of_fp8_peak"] = round(o["tflops"] / (peak_bf16 * FP8_OVER_BF16), 4)
@@ -438,16 +496,23 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the timed kernel from an ncu capture")
+    ap.add_argument("--only", choices=SECONDARY, default=None,
+                    help="time one secondary workload alone (for profiling); prints its line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.only:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        print(json.dumps(secondary_configs(args.steps, args.warmup, (args.only,))[0]))
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

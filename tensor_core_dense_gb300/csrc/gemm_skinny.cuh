@@ -20,14 +20,20 @@
 // per CTA (stream-K), which spreads the B stream (the HBM-bound part) evenly
 // over all SMs.  A tile whose K range is split over several CTAs is finished
 // through a global FP32 workspace: each CTA writes its partial sums to its
-// slot, bumps the tile's counter, and the last one to arrive adds the slots
-// in slot order (deterministic) and writes D.
+// slot as soon as its part is summed, and only at the end of its range (so
+// the pipeline never stops in the middle) bumps the tiles' counters; the last
+// CTA to arrive at a tile adds the slots in slot order (deterministic) and
+// writes D.  Only the first and the last piece of a CTA's range can be
+// partial tiles.
 //
-// Roles (10 warps): warp 0 TMA producer (one lane), warp 1 TMEM allocator +
-// MMA issuer (one lane), warps 2-9 two epilogue warpgroups; warpgroup h
-// promotes columns [h*Mp/2, (h+1)*Mp/2) of every partial.  The MMA writes
-// each K block's partial into one of four TMEM buffers; the epilogue drains
-// it, multiplies by sa*sb and adds it into registers.
+// Roles: warp 0 TMA producer (one lane), warp 1 TMEM allocator + MMA issuer
+// (one lane), then two (Mp <= 32) or four (Mp >= 64) epilogue warpgroups;
+// warpgroup h promotes its own slice of Mp/2 or Mp/4 columns of every
+// partial.  The MMA writes
+// each K block's partial into one of four (Mp = 128) or eight TMEM buffers;
+// the epilogue drains it, multiplies by sa*sb (read from a shared-memory table
+// of the CTA's scale products, filled once with all its loads in flight) and
+// adds it into registers.
 #pragma once
 
 #include <cuda.h>
@@ -38,24 +44,32 @@
 
 namespace tcg {
 
-constexpr int kSkThreads = 320;
-constexpr int kSkNumAcc = 4;                  // TMEM partial buffers
+
 constexpr uint32_t kSkBTileBytes = 128 * 128; // 128 rows of B x 128 K bytes
-constexpr int kSkEpiThreads = 256;
+constexpr int kSkMaxSeg = 4;                  // CTAs sharing one tile, at most
 
 template <int kMp>
 struct SkinnyCfg {
   static constexpr uint32_t kATileBytes = kMp * 128;
   static constexpr uint32_t kStageBytes = kSkBTileBytes + kATileBytes;
-  static constexpr int kStagesRaw = (int)((196u * 1024u) / kStageBytes);
+  // scale-product table: kTabSteps K blocks x kMp columns of sa*sb
+  static constexpr uint32_t kTabBytes = 16u * 1024u;
+  static constexpr int kTabSteps = (int)(kTabBytes / (kMp * 4u));
+  static constexpr int kStagesRaw = (int)((224u * 1024u - kTabBytes - 2048u) / kStageBytes);
   static constexpr int kStages = kStagesRaw > 10 ? 10 : kStagesRaw;
-  static constexpr int kCols = kMp * kSkNumAcc;
+  static constexpr int kNumAcc = kMp >= 128 ? 4 : 8;  // TMEM partial buffers
+  static constexpr int kCols = kMp * kNumAcc;
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
                                    : kCols <= 256 ? 256 : 512;
-  static constexpr int kHalf = kMp / 2;  // columns per epilogue warpgroup
-  static constexpr int kNumBars = 2 * kStages + 2 * kSkNumAcc + 3;
-  static constexpr uint32_t kScaleBytes = 8u * kHalf * 4u;
-  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024u + kScaleBytes + 1024u;
+  // epilogue: kEpiWG warpgroups, warpgroup h promotes columns
+  // [h*kCols, (h+1)*kCols) of every partial
+  static constexpr int kEpiWG = kMp >= 64 ? 4 : 2;
+  static constexpr int kEpiWarps = 4 * kEpiWG;
+  static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kThreads = 64 + kEpiThreads;
+  static constexpr int kHalf = kMp / kEpiWG;  // columns per epilogue warp
+  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 4;
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024u + kTabBytes + 1024u;
   static_assert(kMp % 16 == 0 && kMp >= 16 && kMp <= 128, "UMMA N");
 };
 
@@ -82,14 +96,72 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t x, int64_t T, int64
   return ((x + 1) * G - 1) / T;
 }
 
+// D[m, n] = alpha * val (+ beta * C[m, n]), skipping the padding rows and
+// columns (m >= M, n >= N).
+__device__ __forceinline__ void emit_one(const SkinnyParams& p, int m, int n, float val) {
+  if (m >= p.M || n >= p.N) return;
+  float o = p.alpha * val;
+  if (p.out_f32) {
+    if (p.has_c) o += p.beta * static_cast<const float*>(p.C)[(int64_t)m * p.ldc + n];
+    static_cast<float*>(p.D)[(int64_t)m * p.ldd + n] = o;
+  } else {
+    if (p.has_c)
+      o += p.beta *
+           __uint_as_float((uint32_t)static_cast<const uint16_t*>(p.C)[(int64_t)m * p.ldc + n]
+                           << 16);
+    static_cast<uint16_t*>(p.D)[(int64_t)m * p.ldd + n] =
+        (uint16_t)(pack_bf16x2(o, 0.0f) & 0xFFFFu);
+  }
+}
+
+// Four consecutive outputs D[m, n .. n+3] (n a multiple of 4): one vector
+// store when all four are inside the matrix.
+__device__ __forceinline__ void emit_four(const SkinnyParams& p, int m, int n, float4 v) {
+  if (m >= p.M || n >= p.N) return;
+  if (n + 4 > p.N) {
+    emit_one(p, m, n + 0, v.x);
+    emit_one(p, m, n + 1, v.y);
+    emit_one(p, m, n + 2, v.z);
+    emit_one(p, m, n + 3, v.w);
+    return;
+  }
+  float o[4] = {p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w};
+  if (p.out_f32) {
+    float* d = static_cast<float*>(p.D) + (int64_t)m * p.ldd + n;
+    if (p.has_c) {
+      const float4 c = *reinterpret_cast<const float4*>(static_cast<const float*>(p.C) +
+                                                        (int64_t)m * p.ldc + n);
+      o[0] += p.beta * c.x;
+      o[1] += p.beta * c.y;
+      o[2] += p.beta * c.z;
+      o[3] += p.beta * c.w;
+    }
+    *reinterpret_cast<float4*>(d) = make_float4(o[0], o[1], o[2], o[3]);
+  } else {
+    uint16_t* d = static_cast<uint16_t*>(p.D) + (int64_t)m * p.ldd + n;
+    if (p.has_c) {
+      const uint2 c = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.C) +
+                                                      (int64_t)m * p.ldc + n);
+      o[0] += p.beta * bf16_lo_to_f32(c.x);
+      o[1] += p.beta * bf16_hi_to_f32(c.x);
+      o[2] += p.beta * bf16_lo_to_f32(c.y);
+      o[3] += p.beta * bf16_hi_to_f32(c.y);
+    }
+    *reinterpret_cast<uint2*>(d) = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+  }
+}
+
 template <int kMp>
-__global__ void __launch_bounds__(kSkThreads, 1)
+__global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     gemm_fp8_block_skinny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                  const __grid_constant__ CUtensorMap tmap_b,
                                  const SkinnyParams p) {
   using Cfg = SkinnyCfg<kMp>;
   constexpr int S = Cfg::kStages;
   constexpr int kHalf = Cfg::kHalf;
+  constexpr int kSkNumAcc = Cfg::kNumAcc;
+  constexpr int kSkEpiThreads = Cfg::kEpiThreads;
+  constexpr uint32_t kEpiWarps = Cfg::kEpiWarps;
   constexpr uint32_t kIdesc = make_idesc(0, 0, 128, kMp);  // E4M3 x E4M3 -> F32, M=128, N=Mp
 
   extern __shared__ uint8_t smem_raw[];
@@ -99,8 +171,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * Cfg::kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  float* scale_area = reinterpret_cast<float*>(gbase + S * Cfg::kStageBytes + 1024);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
+  float* stab = reinterpret_cast<float*>(gbase + S * Cfg::kStageBytes + 1024);
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
@@ -108,8 +180,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * S + b); };
   auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * S + kSkNumAcc + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 2 * kSkNumAcc);
-  const uint32_t seg_bar = bar0 + 8u * (2 * S + 2 * kSkNumAcc + 1);   // 8 epilogue warps done
+  const uint32_t seg_bar = bar0 + 8u * (2 * S + 2 * kSkNumAcc + 1);   // epilogue warps done
   const uint32_t flag_bar = bar0 + 8u * (2 * S + 2 * kSkNumAcc + 2);  // last_flag published
+  const uint32_t tab_bar = bar0 + 8u * (2 * S + 2 * kSkNumAcc + 3);   // epilogue group sync
   auto b_smem = [&](uint32_t s) { return sbase + s * Cfg::kStageBytes; };
   auto a_smem = [&](uint32_t s) { return sbase + s * Cfg::kStageBytes + kSkBTileBytes; };
 
@@ -127,13 +200,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     }
     for (int b = 0; b < kSkNumAcc; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 8);  // one arrival per epilogue warp
+      mbar_init(tempty_bar(b), kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain_bar, 1);
-    mbar_init(seg_bar, 8);
+    mbar_init(seg_bar, kEpiWarps);
     mbar_init(flag_bar, 1);
+    mbar_init(tab_bar, kEpiWarps);
     *abort_flag = 0;
-    *last_flag = 0;
+    last_flag[0] = last_flag[1] = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -175,6 +249,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
       }
     }
+    __syncwarp();  // reconverge before the CTA barrier
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -208,117 +283,185 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------- epilogue
-    const uint32_t ew = warp - 2;   // 0..7
+    const uint32_t ew = warp - 2;   // 0 .. kEpiWarps-1
     const uint32_t q = warp & 3u;   // TMEM lane quarter
-    const uint32_t h = ew >> 2;     // column half
+    const uint32_t h = ew >> 2;     // column group
     const int col0 = (int)h * kHalf;
     const int nloc = (int)(q * 32u + lane);
-    float* sc = scale_area + ew * kHalf;  // this warp's scale vector
-    uint32_t j = 0, nsplit = 0;
+    const int etid = (int)(ew * 32u + lane);  // 0 .. kSkEpiThreads-1
+    uint32_t tab_phase = 0;
+    // The epilogue warps meet on an mbarrier with a bounded wait, so a warp
+    // that aborts cannot leave the others blocked.
+    auto group_sync = [&](uint32_t where) -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tab_bar);
+      uint32_t okg = 0;
+      if (lane == 0) okg = wait_phase(tab_bar, tab_phase & 1u, abort_flag, where) ? 1u : 0u;
+      ++tab_phase;
+      return __shfl_sync(0xFFFFFFFFu, okg, 0) != 0;
+    };
+    uint32_t j = 0;
+    int pend_nt[2];  // partial tiles of this range (its first and last piece)
+    int npend = 0;
     bool ok = true;
-    int64_t st = s0;
-    while (ok && st < s1) {
-      const int nt = (int)(st / KB);
-      const int64_t seg_end = ((int64_t)nt + 1) * KB < s1 ? ((int64_t)nt + 1) * KB : s1;
-      const int kb_first = (int)(st - (int64_t)nt * KB);
-      float acc[kHalf];
+    int64_t st = s0, tab_begin = s0, tab_end = s0;
+    float acc[kHalf];
 #pragma unroll
-      for (int c = 0; c < kHalf; ++c) acc[c] = 0.0f;
-      for (; st < seg_end; ++st, ++j) {
-        const int kb = (int)(st - (int64_t)nt * KB);
-        // this K block's column scales sa[kb, m] * sb[nt, kb]
-        const float sbv = p.b_scale[(int64_t)nt * KB + kb];
-        for (int c = (int)lane; c < kHalf; c += 32) {
-          const int m = col0 + c;
-          sc[c] = m < p.M ? p.a_scale[(int64_t)kb * p.M + m] * sbv : 0.0f;
-        }
-        const uint32_t b = j % kSkNumAcc, bph = (j / kSkNumAcc) & 1u;
-        uint32_t got = 0;
-        if (lane == 0) got = wait_phase(tfull_bar(b), bph, abort_flag, 0x14) ? 1u : 0u;
-        got = __shfl_sync(0xFFFFFFFFu, got, 0);
-        if (!got) {
+    for (int c = 0; c < kHalf; ++c) acc[c] = 0.0f;
+    for (; ok && st < s1; ++st, ++j) {
+      if (st == tab_end) {
+        // Next chunk of the scale-product table: every load in flight at once.
+        if (st != s0 && !group_sync(0x17)) {  // everyone is done with the old chunk
           ok = false;
           break;
         }
-        tc_fence_after_sync();
-        uint32_t r[kHalf];
-        tmem_load_cols<kHalf>(tmem_base + ((q * 32u) << 16) + b * kMp + (uint32_t)col0, r);
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(b));
+        tab_begin = st;
+        tab_end = s1 - st < Cfg::kTabSteps ? s1 : st + Cfg::kTabSteps;
+        const int n = (int)(tab_end - tab_begin) * kMp;
+        // 8 entries per thread per round, every load issued before any store
+        for (int base = 0; base < n; base += 8 * kSkEpiThreads) {
+          float va[8], vb[8];
 #pragma unroll
-        for (int c = 0; c < kHalf; c += 4) {
-          const float4 s4 = *reinterpret_cast<const float4*>(sc + c);
-          acc[c + 0] = fmaf(__uint_as_float(r[c + 0]), s4.x, acc[c + 0]);
-          acc[c + 1] = fmaf(__uint_as_float(r[c + 1]), s4.y, acc[c + 1]);
-          acc[c + 2] = fmaf(__uint_as_float(r[c + 2]), s4.z, acc[c + 2]);
-          acc[c + 3] = fmaf(__uint_as_float(r[c + 3]), s4.w, acc[c + 3]);
+          for (int e = 0; e < 8; ++e) {
+            const int idx = base + e * kSkEpiThreads + etid;
+            va[e] = 0.0f;
+            vb[e] = 0.0f;
+            if (idx < n) {
+              const int64_t gst = tab_begin + idx / kMp;
+              const int m = idx % kMp;
+              const int64_t tnt = gst / KB, tkb = gst % KB;
+              if (m < p.M) {
+                va[e] = __ldg(p.a_scale + tkb * p.M + m);
+                vb[e] = __ldg(p.b_scale + tnt * KB + tkb);
+              }
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int idx = base + e * kSkEpiThreads + etid;
+            if (idx < n) stab[idx] = va[e] * vb[e];
+          }
         }
-        __syncwarp();  // sc is rewritten for the next K block
+        if (!group_sync(0x18)) {
+          ok = false;
+          break;
+        }
       }
-      if (!ok) break;
-      // ---- the segment [kb_first, kb_last] of tile nt is summed
-      const int kb_last_excl = (int)(seg_end - (int64_t)nt * KB);
-      const int n = nt * 128 + nloc;
-      auto emit = [&](int m, float val) {
-        if (m >= p.M || n >= p.N) return;
-        float o = p.alpha * val;
-        if (p.out_f32) {
-          if (p.has_c) o += p.beta * static_cast<const float*>(p.C)[(int64_t)m * p.ldc + n];
-          static_cast<float*>(p.D)[(int64_t)m * p.ldd + n] = o;
-        } else {
-          if (p.has_c)
-            o += p.beta * __uint_as_float(
-                              (uint32_t)static_cast<const uint16_t*>(p.C)[(int64_t)m * p.ldc + n]
-                              << 16);
-          static_cast<uint16_t*>(p.D)[(int64_t)m * p.ldd + n] =
-              (uint16_t)(pack_bf16x2(o, 0.0f) & 0xFFFFu);
-        }
-      };
-      if (kb_first == 0 && kb_last_excl == KB) {
+      const int nt = (int)(st / KB);
+      const int kb = (int)(st - (int64_t)nt * KB);
+      const uint32_t b = j % kSkNumAcc, bph = (j / kSkNumAcc) & 1u;
+      uint32_t got = 0;
+      if (lane == 0) got = wait_phase(tfull_bar(b), bph, abort_flag, 0x14) ? 1u : 0u;
+      got = __shfl_sync(0xFFFFFFFFu, got, 0);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const float* sc = stab + (st - tab_begin) * kMp + col0;
+      // Drain the partial in pieces of at most 32 columns (register budget).
+      constexpr int kPiece = kHalf < 32 ? kHalf : 32;
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) emit(col0 + c, acc[c]);
+      for (int c1 = 0; c1 < kHalf; c1 += kPiece) {
+        uint32_t r[kPiece];
+        tmem_load_cols<kPiece>(
+            tmem_base + ((q * 32u) << 16) + b * kMp + (uint32_t)(col0 + c1), r);
+#pragma unroll
+        for (int c = 0; c < kPiece; c += 4) {
+          const float4 s4 = *reinterpret_cast<const float4*>(sc + c1 + c);
+          acc[c1 + c + 0] = fmaf(__uint_as_float(r[c + 0]), s4.x, acc[c1 + c + 0]);
+          acc[c1 + c + 1] = fmaf(__uint_as_float(r[c + 1]), s4.y, acc[c1 + c + 1]);
+          acc[c1 + c + 2] = fmaf(__uint_as_float(r[c + 2]), s4.z, acc[c1 + c + 2]);
+          acc[c1 + c + 3] = fmaf(__uint_as_float(r[c + 3]), s4.w, acc[c1 + c + 3]);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(b));
+      const bool seg_done = kb == KB - 1 || st == s1 - 1;
+      if (!seg_done) continue;
+      // ---- this CTA's K range of tile nt is summed
+      const int64_t tile_first = st - kb;
+      const int kb_first = (int)((tile_first > s0 ? tile_first : s0) - tile_first);
+      if (kb_first == 0 && kb == KB - 1) {
+        const int n = nt * 128 + nloc;
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c) emit_one(p, col0 + c, n, acc[c]);
       } else {
-        const int64_t first_owner = sk_owner((int64_t)nt * KB, T, G);
-        const int64_t last_owner = sk_owner((int64_t)nt * KB + KB - 1, T, G);
-        const int nseg = (int)(last_owner - first_owner + 1);
+        // partial tile: park it in this CTA's workspace slot; the handshake
+        // waits for the end of the range
+        const int64_t first_owner = sk_owner(tile_first, T, G);
         const int slot = (int)((int64_t)blockIdx.x - first_owner);
-        float* wsp = p.ws + ((int64_t)nt * p.max_seg + slot) * (int64_t)kMp * 128;
+        float* wsp = p.ws + ((int64_t)nt * p.max_seg + slot) * kMp * 128;
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) __stcg(wsp + (int64_t)(col0 + c) * 128 + nloc, acc[c]);
-        // Publish the partial, then one thread counts arrivals for the tile.
-        // The group syncs through mbarriers with bounded waits, so an
-        // aborting warp cannot leave the others blocked.
+        pend_nt[npend++] = nt;
+      }
+#pragma unroll
+      for (int c = 0; c < kHalf; ++c) acc[c] = 0.0f;
+    }
+    // ---- end of the range: count this CTA's partial tiles in, and finish
+    // the tiles it is the last contributor to.
+    if (ok && npend > 0) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(seg_bar);
+      if (ew == 0 && lane < (uint32_t)npend) {
+        const int tnt = pend_nt[lane];
+        const int64_t tf = (int64_t)tnt * KB;
+        const int nseg = (int)(sk_owner(tf + KB - 1, T, G) - sk_owner(tf, T, G) + 1);
+        int last = 0;
+        if (wait_phase(seg_bar, 0, abort_flag, 0x15)) {
+          const unsigned prev = atomicAdd(&p.counters[tnt], 1u);
+          last = prev == (unsigned)(nseg - 1);
+          if (last) p.counters[tnt] = 0u;  // ready for the next call
+        }
+        last_flag[lane] = last;
+      }
+      __syncwarp();
+      if (ew == 0 && lane == 0) mbar_arrive(flag_bar);
+      uint32_t gotf = 0;
+      if (lane == 0) gotf = wait_phase(flag_bar, 0, abort_flag, 0x16) ? 1u : 0u;
+      gotf = __shfl_sync(0xFFFFFFFFu, gotf, 0);
+      if (gotf && !*abort_flag) {
         __threadfence();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(seg_bar);
-        const uint32_t par = nsplit & 1u;
-        ++nsplit;
-        if (ew == 0 && lane == 0) {
-          int last = 0;
-          if (wait_phase(seg_bar, par, abort_flag, 0x15)) {
-            const unsigned prev = atomicAdd(&p.counters[nt], 1u);
-            last = prev == (unsigned)(nseg - 1);
-            if (last) p.counters[nt] = 0u;  // ready for the next call
-          }
-          *last_flag = last;
-          mbar_arrive(flag_bar);
-        }
-        uint32_t got = 0;
-        if (lane == 0) got = wait_phase(flag_bar, par, abort_flag, 0x16) ? 1u : 0u;
-        got = __shfl_sync(0xFFFFFFFFu, got, 0);
-        if (!got || *abort_flag) {
-          ok = false;
-          break;
-        }
-        if (*last_flag) {
-          __threadfence();
-          const float* wt = p.ws + (int64_t)nt * p.max_seg * kMp * 128;
-          for (int c = 0; c < kHalf; ++c) {
-            float sum = 0.0f;
-            for (int sgi = 0; sgi < nseg; ++sgi)
-              sum += __ldcg(wt + ((int64_t)sgi * kMp + col0 + c) * 128 + nloc);
-            emit(col0 + c, sum);
+        for (int i = 0; i < npend; ++i) {
+          if (!last_flag[i]) continue;
+          const int tnt = pend_nt[i];
+          const int64_t tf = (int64_t)tnt * KB;
+          const int nseg = (int)(sk_owner(tf + KB - 1, T, G) - sk_owner(tf, T, G) + 1);
+          const float* wt = p.ws + (int64_t)tnt * p.max_seg * kMp * 128;
+          // All epilogue threads sum the slots (in slot order) over float4
+          // units of the Mp x 128 tile: a warp covers 32 consecutive units (one
+          // row m), kU units x all slots in flight per thread.
+          constexpr int kUnits = kMp * 32;  // float4 units per slot
+          constexpr int kU = kMp >= 64 ? 4 : 2;
+          static_assert(kUnits % (kSkEpiThreads * kU) == 0, "reduction tiling");
+          for (int u0 = 0; u0 < kUnits; u0 += kSkEpiThreads * kU) {
+            float4 part[kSkMaxSeg][kU];
+#pragma unroll
+            for (int sgi = 0; sgi < kSkMaxSeg; ++sgi)
+#pragma unroll
+              for (int v = 0; v < kU; ++v)
+                part[sgi][v] = sgi < nseg
+                                   ? __ldcg(reinterpret_cast<const float4*>(wt) +
+                                            (int64_t)sgi * kUnits + u0 + v * kSkEpiThreads + etid)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int v = 0; v < kU; ++v) {
+              float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int sgi = 0; sgi < kSkMaxSeg; ++sgi) {
+                if (sgi < nseg) {
+                  sum.x += part[sgi][v].x;
+                  sum.y += part[sgi][v].y;
+                  sum.z += part[sgi][v].z;
+                  sum.w += part[sgi][v].w;
+                }
+              }
+              const int u = u0 + v * kSkEpiThreads + etid;
+              emit_four(p, u >> 5, tnt * 128 + (u & 31) * 4, sum);
+            }
           }
         }
       }

@@ -333,7 +333,25 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   const int64_t T = (int64_t)p.n_tiles * p.num_kb;
   if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
   p.total_steps = (int32_t)T;
-  p.grid = (int32_t)(T < sms ? T : sms);
+  // With fewer N tiles than SMs, each tile's K range is cut into
+  // floor(SMs / tiles) equal pieces (at most 3), one per CTA, so a tile has
+  // few partial sums to add; otherwise the steps are spread over all SMs and
+  // every CTA gets at least ceil(KB/3) of them.  Either way at most kSkMaxSeg
+  // (4) CTAs share a tile.
+  {
+    int64_t g;
+    if (p.n_tiles < sms) {
+      int64_t split = sms / p.n_tiles;
+      if (split > 3) split = 3;
+      if (split > p.num_kb) split = p.num_kb;
+      g = p.n_tiles * split;
+    } else {
+      const int64_t min_steps = (p.num_kb + 2) / 3;
+      g = T / min_steps;
+      if (g > sms) g = sms;
+    }
+    p.grid = (int32_t)(g < 1 ? 1 : g);
+  }
   // Segments per tile: a tile of num_kb steps meets at most
   // ceil(num_kb / min_range) + 1 ranges, min_range = floor(T / grid).
   const int64_t min_range = T / p.grid;
@@ -358,7 +376,7 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   }
   auto* fn = &gemm_fp8_block_skinny_kernel<kMp>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
-  fn<<<p.grid, kSkThreads, Cfg::kSmemBytes, stream>>>(ma, mb, p);
+  fn<<<p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(ma, mb, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
@@ -509,7 +527,25 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
   const int64_t T = (int64_t)p.n_tiles * p.num_kb;
   if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
   p.total_steps = (int32_t)T;
-  p.grid = (int32_t)(T < sms ? T : sms);
+  // With fewer N tiles than SMs, each tile's K range is cut into
+  // floor(SMs / tiles) equal pieces (at most 3), one per CTA, so a tile has
+  // few partial sums to add; otherwise the steps are spread over all SMs and
+  // every CTA gets at least ceil(KB/3) of them.  Either way at most kSkMaxSeg
+  // (4) CTAs share a tile.
+  {
+    int64_t g;
+    if (p.n_tiles < sms) {
+      int64_t split = sms / p.n_tiles;
+      if (split > 3) split = 3;
+      if (split > p.num_kb) split = p.num_kb;
+      g = p.n_tiles * split;
+    } else {
+      const int64_t min_steps = (p.num_kb + 2) / 3;
+      g = T / min_steps;
+      if (g > sms) g = sms;
+    }
+    p.grid = (int32_t)(g < 1 ? 1 : g);
+  }
   const int64_t min_range = T / p.grid;
   p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);
   if (p.max_seg > p.grid) p.max_seg = p.grid;
@@ -548,7 +584,7 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
       raised[dev] = true;
     }
   }
-  fn<<<p.grid, kSkThreads, Cfg::kSmemBytes, stream>>>(ma, mb, p);
+  fn<<<p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(ma, mb, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
