@@ -7,12 +7,14 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
 
 #include "gemm_skinny.cuh"
 #include "gemm_tn.cuh"
+#include "gemm_tn2.cuh"
 #include "tcgemm.h"
 
 namespace tcg {
@@ -250,12 +252,107 @@ tcg_status launch_tn_inst(const CUtensorMap& ma, const CUtensorMap& mb, const Ge
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
 
+// Kernel choice for the dense path: the CTA-pair kernel for problems with at
+// least one full 256 x 256 tile, else the one-SM kernel.  TCG_KERNEL=1cta or
+// 2cta in the environment forces one of them (for tests and measurements).
+int forced_kernel() {
+  static int v = [] {
+    const char* e = std::getenv("TCG_KERNEL");
+    if (!e) return 0;
+    if (std::strcmp(e, "1cta") == 0) return 1;
+    if (std::strcmp(e, "2cta") == 0) return 2;
+    return 0;
+  }();
+  return v;
+}
+
+template <int kIn, int kOut, bool kHasC>
+tcg_status launch_tn2_inst(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm2Params& p,
+                           int grid, int dev, cudaStream_t stream) {
+  auto* fn = &gemm_tn2_kernel<kIn, kOut, kHasC>;
+  if (tcg_status s = ensure_smem(fn, kP2SmemBytes, dev); s != TCG_OK) return s;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kP2SmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fn, ma, mb, p) != cudaSuccess) return TCG_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+// The persistent 256 x 256 pair-tile kernel.
+template <int kIn>
+tcg_status launch_tn2(const Common& a, const float* a_scale, const float* b_scale,
+                      cudaStream_t stream, int dev, int sms) {
+  const int in_bytes = kIn == 0 ? 2 : 1;
+  const CUtensorMapDataType dt =
+      kIn == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint32_t box_k = kBKBytes / in_bytes;
+  CUtensorMap ma, mb;
+  if (tcg_status s = tensor_map(&ma, dt, a.A, a.K, a.M, a.lda * in_bytes, box_k, 128); s != TCG_OK)
+    return s;
+  if (tcg_status s = tensor_map(&mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, box_k, kBBoxRows);
+      s != TCG_OK)
+    return s;
+  Gemm2Params p{};
+  p.M = (int32_t)a.M;
+  p.N = (int32_t)a.N;
+  p.K = (int32_t)a.K;
+  p.tiles_m = (int32_t)((a.M + 255) / 256);
+  p.tiles_n = (int32_t)((a.N + 255) / 256);
+  p.num_kb = (int32_t)((a.K * in_bytes + kBKBytes - 1) / kBKBytes);
+  const int64_t tiles = (int64_t)p.tiles_m * p.tiles_n;
+  if (tiles > INT32_MAX) return TCG_ERR_UNSUPPORTED;
+  p.num_tiles = (int32_t)tiles;
+  const int clusters_max = sms / 2;
+  int clusters;
+  int64_t rest;
+  if (tiles >= clusters_max) {
+    clusters = clusters_max;
+    p.dp_waves = (int32_t)(tiles / clusters_max);
+    rest = tiles % clusters_max;
+  } else {
+    p.dp_waves = 0;
+    rest = tiles;
+  }
+  const int split = (rest > 0 && rest * 2 <= clusters_max) ? 2 : 1;
+  if (tiles < clusters_max) clusters = (int)(rest * split);
+  p.dp_end = (int32_t)(tiles - rest);
+  p.split = split;
+  p.C = a.beta != 0.0f ? a.C : nullptr;
+  p.ldc = a.ldc;
+  p.D = a.D;
+  p.ldd = a.ldd;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.a_scale = a_scale;
+  p.b_scale = b_scale;
+  const int grid = 2 * clusters;
+  const bool has_c = a.beta != 0.0f;
+  if (a.out == TCG_OUT_BF16)
+    return has_c ? launch_tn2_inst<kIn, 0, true>(ma, mb, p, grid, dev, stream)
+                 : launch_tn2_inst<kIn, 0, false>(ma, mb, p, grid, dev, stream);
+  return has_c ? launch_tn2_inst<kIn, 1, true>(ma, mb, p, grid, dev, stream)
+               : launch_tn2_inst<kIn, 1, false>(ma, mb, p, grid, dev, stream);
+}
+
 // The persistent 128 x 256 tile kernel (BF16, or per-tensor FP8).
 template <int kIn>
 tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale,
                      cudaStream_t stream) {
   int dev, sms;
   if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+  const int fk = forced_kernel();
+  if (fk == 2 || (fk == 0 && a.M >= 256 && a.N >= 256))
+    return launch_tn2<kIn>(a, a_scale, b_scale, stream, dev, sms);
   const int in_bytes = kIn == 0 ? 2 : 1;
   const CUtensorMapDataType dt =
       kIn == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
