@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dependency_wait();  // global memory only after the previous kernel finished
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
         tma_load_2d_hint(b_smem(s), &tmap_b, full_bar(s), kb * 128, nt * 128, stream_policy);
         tma_load_2d_hint(a_smem(s), &tmap_a, full_bar(s), kb * 128, 0, keep_policy);
       }
+      grid_launch_dependents();  // every load is issued: the next kernel may launch
       if (!ok) {
         const uint32_t n = j < (uint32_t)S ? j : (uint32_t)S;
         for (uint32_t i = j - n; i < j; ++i) {

@@ -295,6 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // The set-up above may overlap the previous kernel's tail; global memory
+  // is touched only after it has finished.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer
@@ -325,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kb * kBKElems, brow0 + bx * kBBoxRows);
         }
       }
+      grid_launch_dependents();  // every load is issued: the next kernel may launch
       if (!ok) {
         // Let the copies already issued land before the CTA can exit.
         const uint32_t n = it < (uint32_t)kStages ? it : (uint32_t)kStages;

@@ -31,7 +31,7 @@
 
 namespace tcg {
 
-constexpr int kP2Stages = 6;
+constexpr int kP2Stages = 7;
 constexpr uint32_t kP2ATileBytes = 128 * kBKBytes;  // this CTA's 128 rows of A
 constexpr uint32_t kP2BTileBytes = 128 * kBKBytes;  // up to 128 rows of B (its half)
 constexpr uint32_t kP2StageBytes = kP2ATileBytes + kP2BTileBytes;
@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // the peer's barriers are initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dependency_wait();  // global memory only after the previous kernel finished
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              kb * kBKElems, brow0 + bx * kBBoxRows);
         }
       }
+      grid_launch_dependents();  // every load is issued: the next kernel may launch
     }
     __syncwarp();
   } else if (warp == 1) {

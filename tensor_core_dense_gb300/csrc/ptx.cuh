@@ -67,6 +67,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// ------------------------------------------------- programmatic launch
+
+// Waits until the grids this one depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialisation) have finished
+// and their memory is visible.  A no-op otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream start launching (its CTAs take SMs as
+// this grid's CTAs exit) before this grid has finished.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include "gemm_skinny.cuh"
 #include "gemm_tn.cuh"
@@ -242,12 +243,42 @@ tcg_status launch_k0(const Common& a, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
 
+// Launches a GEMM kernel with programmatic stream serialisation, so that its
+// CTAs may start (and run their set-up) while the previous kernel in the
+// stream drains; the kernels wait for that kernel before touching global
+// memory.  cluster_x > 1 launches clusters of that many CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_gemm_kernel(void (*fn)(KArgs...), int grid, int block, uint32_t smem,
+                               cudaStream_t stream, int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelEx(&cfg, fn, std::forward<Args>(args)...);
+}
+
 template <int kIn, int kOut, bool kHasC>
 tcg_status launch_tn_inst(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                           int grid, int dev, cudaStream_t stream) {
   auto* fn = &gemm_tn_kernel<kIn, kOut, kHasC>;
   if (tcg_status s = ensure_smem(fn, kSmemBytes, dev); s != TCG_OK) return s;
-  fn<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+  if (launch_gemm_kernel(fn, grid, kThreads, kSmemBytes, stream, 1, ma, mb, p) != cudaSuccess)
+    return TCG_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
@@ -256,14 +287,11 @@ tcg_status launch_tn_inst(const CUtensorMap& ma, const CUtensorMap& mb, const Ge
 // least one full 256 x 256 tile, else the one-SM kernel.  TCG_KERNEL=1cta or
 // 2cta in the environment forces one of them (for tests and measurements).
 int forced_kernel() {
-  static int v = [] {
-    const char* e = std::getenv("TCG_KERNEL");
-    if (!e) return 0;
-    if (std::strcmp(e, "1cta") == 0) return 1;
-    if (std::strcmp(e, "2cta") == 0) return 2;
-    return 0;
-  }();
-  return v;
+  const char* e = std::getenv("TCG_KERNEL");
+  if (!e) return 0;
+  if (std::strcmp(e, "1cta") == 0) return 1;
+  if (std::strcmp(e, "2cta") == 0) return 2;
+  return 0;
 }
 
 template <int kIn, int kOut, bool kHasC>
@@ -271,19 +299,8 @@ tcg_status launch_tn2_inst(const CUtensorMap& ma, const CUtensorMap& mb, const G
                            int grid, int dev, cudaStream_t stream) {
   auto* fn = &gemm_tn2_kernel<kIn, kOut, kHasC>;
   if (tcg_status s = ensure_smem(fn, kP2SmemBytes, dev); s != TCG_OK) return s;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kP2SmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, fn, ma, mb, p) != cudaSuccess) return TCG_ERR_CUDA;
+  if (launch_gemm_kernel(fn, grid, kThreads, kP2SmemBytes, stream, 2, ma, mb, p) != cudaSuccess)
+    return TCG_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
@@ -473,7 +490,9 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   }
   auto* fn = &gemm_fp8_block_skinny_kernel<kMp>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
-  fn<<<p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(ma, mb, p);
+  if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 1, ma, mb, p) !=
+      cudaSuccess)
+    return TCG_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }

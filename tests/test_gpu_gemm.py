@@ -117,6 +117,24 @@ def test_tail_schedules(M, N, K, kind, out, beta):
     check_full(w, run(w))
 
 
+# Both dense kernels on every kind of shape: the one-SM 128 x 256 kernel and
+# the CTA-pair 256 x 256 kernel (the library picks one by shape; TCG_KERNEL
+# forces either).
+@pytest.mark.parametrize("kernel", ["1cta", "2cta"])
+@pytest.mark.parametrize("M,N,K,kind,out,beta", [
+    (1, 8, 8, "bf16", "f32", 0.0), (129, 257, 65, "bf16", "bf16", 1.0),
+    (1000, 1000, 2048, "fp8", "bf16", 0.0), (2048, 2560, 1024, "bf16", "f32", -0.5),
+    (4096, 2560, 512, "fp8", "f32", 0.0), (777, 3000, 1111, "bf16", "bf16", 1.0),
+    (2048, 4096, 512, "bf16", "f32", 0.0)])
+def test_dense_kernels_both_paths(monkeypatch, kernel, M, N, K, kind, out, beta):
+    monkeypatch.setenv("TCG_KERNEL", kernel)
+    if kind == "bf16":
+        w = bf16_case(M, N, K, seed=M + N + 5 * K, out=out, beta=beta)
+    else:
+        w = fp8_case(M, N, K, seed=M + N + 5 * K, mode="tensor", out=out, beta=beta)
+    check_full(w, run(w))
+
+
 def test_tail_schedule_deterministic():
     w = bf16_case(1100, 1300, 4096, seed=4, out="f32")
     d1, d2 = d_to_host(run(w)), d_to_host(run(w))
