@@ -52,7 +52,7 @@ def kernel_source_sha():
     return h.hexdigest()
 
 
-def stored_traffic(summary="gemm_tn_bf16_4096.md"):
+def stored_traffic(summary="gemm_tn2_bf16_4096.md"):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     summary is missing or was taken on different kernel sources."""
     path = os.path.join(ROOT, "profiles", summary)
@@ -161,6 +161,12 @@ def _barrier_max(value, world):
                      device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tflops(flops_per_step, steps, max_total_ms, world):
+    """Whole-job throughput: every rank ran `steps` steps of `flops_per_step`;
+    the job took the slowest rank's time."""
+    return world * flops_per_step * steps / (max_total_ms * 1e-3) / 1e12
 
 
 def _barrier(world):
@@ -356,7 +362,7 @@ def run_ours(args):
 
     total_ms = _barrier_max(total_ms, world)
     ms_per_step = total_ms / args.steps
-    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = aggregate_tflops(w.flops, args.steps, total_ms, world)
 
     # end to end through the public API with host buffers: H2D of A and B from
     # pinned memory, the GEMM, D2H of D, every step (plain calls, no graph)
@@ -412,7 +418,7 @@ def run_ours(args):
                      "peak": peak_bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_bf16, 4),
                      "peak_source": f"{peak_src} bf16_tflops (burst)",
-                     "kernel": "gemm_tn_kernel<bf16,bf16 out>",
+                     "kernel": "gemm_tn2_kernel<bf16,bf16 out> (CTA pair)",
                      "traffic": stored_traffic() if args.traffic is None else args.traffic},
         "gpu_launches": launches,
         "clocks": clocks,

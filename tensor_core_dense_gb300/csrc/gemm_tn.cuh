@@ -295,15 +295,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  // The set-up above may overlap the previous kernel's tail; global memory
-  // is touched only after it has finished.
-  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_a);
       tma_prefetch_desc(&tmap_b);
+      {  // warm L2 with the first stages while the previous kernel drains
+        WorkIter wi;
+        wi.init(p);
+        WorkItem w;
+        if (wi.next(w)) {
+          int tm, tn;
+          tile_coords(w.tile, p.tiles_m, p.tiles_n, tm, tn);
+          const int nboxes = (kBN / kBBoxRows) / w.split;
+          const int brow0 = tn * kBN + w.sub * (kBN / w.split);
+          for (int kb = 0; kb < kStages && kb < p.num_kb; ++kb) {
+            tma_prefetch_l2_2d(&tmap_a, kb * kBKElems, tm * kBM);
+            for (int bx = 0; bx < nboxes; ++bx)
+              tma_prefetch_l2_2d(&tmap_b, kb * kBKElems, brow0 + bx * kBBoxRows);
+          }
+        }
+      }
+    }
+  }
+  // The set-up above may overlap the previous kernel's tail; global memory
+  // is read or written only after it has finished.
+  grid_dependency_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
       WorkIter wi;

@@ -157,13 +157,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // the peer's barriers are initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    // warm L2 with this CTA's first stages while the previous kernel drains
+    PairWorkIter wi;
+    wi.init(p, cluster, clusters);
+    WorkItem w;
+    if (wi.next(w)) {
+      int tm, tn;
+      tile_coords(w.tile, p.tiles_m, p.tiles_n, tm, tn);
+      const int nsub = 256 / w.split, half = nsub / 2;
+      const int brow0 = tn * 256 + w.sub * nsub + (int)rank * half;
+      const int arow0 = tm * 256 + (int)rank * 128;
+      for (int kb = 0; kb < S && kb < p.num_kb; ++kb) {
+        tma_prefetch_l2_2d(&tmap_a, kb * kBKElems, arow0);
+        for (int bx = 0; bx < half / kBBoxRows; ++bx)
+          tma_prefetch_l2_2d(&tmap_b, kb * kBKElems, brow0 + bx * kBBoxRows);
+      }
+    }
+  }
   grid_dependency_wait();  // global memory only after the previous kernel finished
 
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_a);
-      tma_prefetch_desc(&tmap_b);
       uint32_t it = 0;
       bool ok = true;
       PairWorkIter wi;

@@ -110,6 +110,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* map, 
       : "memory");
 }
 
+// Hint: bring one box of a tensor into L2 (no shared memory, no barrier).
+// L2 is coherent for the whole GPU, so this is safe before the grid
+// dependency wait even if the previous kernel is still writing the tensor.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
