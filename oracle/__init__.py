@@ -16,7 +16,11 @@ with gcc and marshals numpy arrays.  Sources and readings:
 * E4M3 = 1/4/3 bits, no infinity, max normal 448, hence bias 7 ("Tensor cores
   and low precision", the FP8 paragraph);
 * FP8 scale factors applied after the product ("Tensor cores and low
-  precision", the scaling paragraph), per tensor or per 128-wide K block.
+  precision", the scaling paragraph), per tensor or per 128-wide K block;
+* the FP8 quantiser that produces those scales and codes: scale = amax / 448
+  per tensor, per 1 x 128 row block or per 128 x 128 block ("Tensor cores and
+  low precision", the scaling paragraph; "Tensor Cores", "Precision: FP16,
+  BF16, TF32, FP8": scaling factors per tensor, per row or per block).
 
 Every function here is pinned by ``tests/test_oracle.py`` against facts the
 pages fix, closed forms, library routines (torch's bfloat16 / float8_e4m3fn
@@ -40,6 +44,7 @@ _lock = threading.Lock()
 _lib = None
 
 IN_BF16, IN_E4M3 = 0, 1
+Q_TENSOR, Q_ROW128, Q_BLOCK128 = 0, 1, 2
 SCALE_NONE, SCALE_TENSOR, SCALE_BLOCK128 = 0, 1, 2
 C_BF16, C_F32 = 0, 1
 
@@ -97,6 +102,10 @@ def _load():
         lib.orc_gemm_tiles.argtypes = [ctypes.POINTER(_Args), ctypes.c_int64, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.orc_gemm_tiles.restype = ctypes.c_int
+        i64 = ctypes.c_int64
+        lib.orc_quant_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_int32, i64, i64, i64,
+                                       ctypes.c_int32, ctypes.c_void_p, i64, ctypes.c_void_p]
+        lib.orc_quant_e4m3.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -206,3 +215,30 @@ def gemm(M, N, K, A, lda, B, ldb, *, in_type=IN_BF16, scale_mode=SCALE_NONE,
     if whole:
         return outs_v[0], outs_b[0]
     return outs_v, outs_b
+
+
+def quantize_e4m3(x, mode, *, ldq=None):
+    """FP8 E4M3 quantisation of a 2-D array x (float32 values, or uint16 BF16
+    bit patterns) with scale = amax / 448 per block (``oracle.c``,
+    orc_quant_e4m3).
+
+    mode: Q_TENSOR (scale[0]), Q_ROW128 (scale[kb*rows + r]) or Q_BLOCK128
+    (scale[rb*ceil(cols/128) + kb]).  Returns (q, scale): q is a rows x ldq
+    uint8 array (columns >= cols stay zero), scale a float32 array.
+    """
+    if x.dtype == np.uint16:
+        x_type = 1
+    else:
+        x_type = 0
+        x = np.asarray(x, dtype=np.float32)
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    ldq = cols if ldq is None else ldq
+    KB, RB = (cols + 127) // 128, (rows + 127) // 128
+    n = {Q_TENSOR: 1, Q_ROW128: KB * rows, Q_BLOCK128: RB * KB}[mode]
+    q = np.zeros((rows, ldq), dtype=np.uint8)
+    s = np.zeros(max(n, 1), dtype=np.float32)
+    rc = _load().orc_quant_e4m3(_ptr(x), x_type, rows, cols, cols, mode, _ptr(q), ldq, _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle rejected the quantiser arguments")
+    return q, s[:n]

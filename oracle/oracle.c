@@ -327,3 +327,86 @@ int orc_gemm_tiles(const orc_gemm_args* g, int64_t ntiles, const int64_t* tiles,
   free(offs);
   return w.err;
 }
+
+/* --------------------------------------------------------------- quantiser */
+
+/* FP8 E4M3 quantisation of a rows x cols matrix X ("Tensor cores and low
+ * precision", FP8 paragraph: rescale so that the largest magnitudes land at
+ * the format's maximum, 448, then cast; the scale is removed again after the
+ * product; "Tensor Cores", "Precision: FP16, BF16, TF32, FP8": the scaling
+ * factors are per tensor, per row or per block).  Written as the library stores it: the
+ * stored (dequantisation) scale is s = amax / 448 and each code is
+ * E4M3(x / s), i.e. the same as multiplying by 448 / amax up to the rounding
+ * of that factor.
+ *
+ * Readings (the pages give the recipe, not these details):
+ *  - amax is the largest |x| over the block, NaN entries ignored;
+ *  - s = amax / 448 in FP32 (correctly rounded division); a block whose s is
+ *    0 (all zeros, or so small that the division underflows) takes s = 1, so
+ *    that no code divides by zero;
+ *  - each code is the FP32 quotient x / s (correctly rounded) encoded to E4M3
+ *    with nearest-even rounding, saturating at +-448 (orc_e4m3_encode); a NaN
+ *    quotient is stored as the canonical NaN code 0x7F.
+ *
+ * Block geometries (mode), matching the GEMM's scale layouts:
+ *  ORC_Q_TENSOR    one block, the whole matrix; scale[0]
+ *  ORC_Q_ROW128    1 x 128: row r, columns 128kb..128kb+127; scale[kb*rows + r]
+ *  ORC_Q_BLOCK128  128 x 128: rows 128rb.., columns 128kb..;
+ *                  scale[rb*ceil(cols/128) + kb]
+ * A partial last block (cols or rows not a multiple of 128) uses its own
+ * amax.  X is FP32 (x_type 0) or BF16 bit patterns (x_type 1), element (r, c)
+ * at X[r*ldx + c]; Q holds one byte per element at Q[r*ldq + c]; bytes of Q
+ * beyond column cols are not written.  Returns 0, or -1 on a bad argument. */
+#define ORC_Q_TENSOR 0
+#define ORC_Q_ROW128 1
+#define ORC_Q_BLOCK128 2
+
+static float quant_in(const void* X, int32_t x_type, int64_t idx) {
+  if (x_type == 0) return ((const float*)X)[idx];
+  return (float)orc_bf16_decode(((const uint16_t*)X)[idx]); /* exact: BF16 is FP32's top half */
+}
+
+/* Quantise the block rows r0..r1-1 x columns c0..c1-1; returns its scale. */
+static float quant_block(const void* X, int32_t x_type, int64_t ldx, int64_t r0, int64_t r1,
+                         int64_t c0, int64_t c1, uint8_t* Q, int64_t ldq) {
+  float amax = 0.0f;
+  for (int64_t r = r0; r < r1; ++r)
+    for (int64_t c = c0; c < c1; ++c) {
+      float a = fabsf(quant_in(X, x_type, r * ldx + c));
+      if (a > amax) amax = a; /* false for NaN: NaN entries are skipped */
+    }
+  float s = amax / 448.0f;
+  if (s == 0.0f) s = 1.0f;
+  for (int64_t r = r0; r < r1; ++r)
+    for (int64_t c = c0; c < c1; ++c) {
+      float y = quant_in(X, x_type, r * ldx + c) / s;
+      Q[r * ldq + c] = (y != y) ? (uint8_t)0x7Fu : orc_e4m3_encode(y);
+    }
+  return s;
+}
+
+int orc_quant_e4m3(const void* X, int32_t x_type, int64_t rows, int64_t cols, int64_t ldx,
+                   int32_t mode, uint8_t* Q, int64_t ldq, float* scale) {
+  if (rows < 0 || cols < 0 || (x_type != 0 && x_type != 1) || !scale) return -1;
+  if (rows > 0 && cols > 0 && (!X || !Q || ldx < cols || ldq < cols)) return -1;
+  const int64_t KB = (cols + 127) / 128, RB = (rows + 127) / 128;
+  if (mode == ORC_Q_TENSOR) {
+    scale[0] = quant_block(X, x_type, ldx, 0, rows, 0, cols, Q, ldq);
+  } else if (mode == ORC_Q_ROW128) {
+    for (int64_t r = 0; r < rows; ++r)
+      for (int64_t kb = 0; kb < KB; ++kb) {
+        int64_t c1 = (kb + 1) * 128 < cols ? (kb + 1) * 128 : cols;
+        scale[kb * rows + r] = quant_block(X, x_type, ldx, r, r + 1, kb * 128, c1, Q, ldq);
+      }
+  } else if (mode == ORC_Q_BLOCK128) {
+    for (int64_t rb = 0; rb < RB; ++rb)
+      for (int64_t kb = 0; kb < KB; ++kb) {
+        int64_t r1 = (rb + 1) * 128 < rows ? (rb + 1) * 128 : rows;
+        int64_t c1 = (kb + 1) * 128 < cols ? (kb + 1) * 128 : cols;
+        scale[rb * KB + kb] = quant_block(X, x_type, ldx, rb * 128, r1, kb * 128, c1, Q, ldq);
+      }
+  } else {
+    return -1;
+  }
+  return 0;
+}

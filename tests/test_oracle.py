@@ -337,3 +337,150 @@ def test_bf16_error_bound_sanity_against_float32_gemm():
     bad[i, j] = v[i, j] + 2 * tol[i, j]
     assert not (np.abs(bad - v) <= tol).all()
     assert math.isfinite(float(v.sum()))
+
+
+# ------------------------------------------------------------------ quantiser
+#
+# The FP8 recipe ("Tensor cores and low precision", scaling paragraph): scale
+# so the largest magnitude sits at 448, cast, remove the scale after the
+# product; scales per tensor, per row (1 x 128) or per block (128 x 128)
+# ("Tensor Cores", "Precision: FP16, BF16, TF32, FP8").
+
+Q_MODES = (oracle.Q_TENSOR, oracle.Q_ROW128, oracle.Q_BLOCK128)
+Q_SHAPES = [(1, 1), (3, 130), (128, 128), (130, 257), (257, 384), (64, 1000)]
+
+
+def _block_ids(rows, cols, mode):
+    """Scale index of every element, from the layouts the GEMM reads."""
+    r = np.arange(rows)[:, None]
+    c = np.arange(cols)[None, :]
+    KB = (cols + 127) // 128
+    if mode == oracle.Q_TENSOR:
+        return np.zeros((rows, cols), dtype=np.int64)
+    if mode == oracle.Q_ROW128:
+        return (c // 128) * rows + r
+    return (r // 128) * KB + (c // 128)
+
+
+def _nblocks(rows, cols, mode):
+    KB, RB = (cols + 127) // 128, (rows + 127) // 128
+    return {oracle.Q_TENSOR: 1, oracle.Q_ROW128: rows * KB, oracle.Q_BLOCK128: RB * KB}[mode]
+
+
+@pytest.mark.parametrize("mode", Q_MODES)
+@pytest.mark.parametrize("rows,cols", Q_SHAPES)
+@pytest.mark.parametrize("bf16_in", [False, True])
+def test_quant_power_of_two_blocks_reproduce_codes_and_scales(mode, rows, cols, bf16_in):
+    # X = decode(code) * 2^p_block with a +-448 in every block: the scale is
+    # exactly 2^p_block and every code comes back unchanged.  A wrong block
+    # geometry, scale index, missing |.| or misplaced division changes bits.
+    rng = np.random.default_rng(rows * 1000 + cols + 7 * mode)
+    codes = rng.integers(0, 256, size=(rows, cols)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3A
+    ids = _block_ids(rows, cols, mode)
+    nb = _nblocks(rows, cols, mode)
+    p = rng.integers(-20, 21, size=nb)
+    flat_ids = ids.ravel()
+    for b in range(nb):  # one +-448 per block, at a random member
+        members = np.flatnonzero(flat_ids == b)
+        codes.flat[rng.choice(members)] = rng.choice([0x7E, 0xFE])
+    x = (oracle.e4m3_decode(codes) * np.exp2(p[ids])).astype(np.float32)
+    if bf16_in:  # E4M3 values times powers of two are exact in BF16
+        xin = oracle.bf16_encode(x)
+        assert np.array_equal(oracle.bf16_decode(xin).astype(np.float32), x)
+    else:
+        xin = x
+    q, s = oracle.quantize_e4m3(xin, mode)
+    assert np.array_equal(s, np.exp2(p).astype(np.float32))
+    assert np.array_equal(q, codes)
+
+
+@pytest.mark.parametrize("mode", Q_MODES)
+def test_quant_block_maximum_lands_on_448_and_zero_block_scale_one(mode):
+    rows, cols = 300, 520
+    x = synth.values_f32(11, 1, rows, cols, out_prob=0.01, out_factor=50.0)
+    x[:128, :128] = 0.0          # an all-zero 128 x 128 block (and 1 x 128 blocks)
+    if mode == oracle.Q_TENSOR:
+        x[:, :] = x * 3.0
+    q, s = oracle.quantize_e4m3(x, mode)
+    ids = _block_ids(rows, cols, mode)
+    dq = np.abs(oracle.e4m3_decode(q))
+    for b in range(_nblocks(rows, cols, mode)):
+        m = ids == b
+        amax = np.abs(x[m]).max()
+        if amax == 0.0:
+            assert s[b] == 1.0 and (q[m] == 0).all()
+        else:
+            assert dq[m].max() == 448.0                      # the largest sits at 448
+            assert abs(float(s[b]) * 448.0 / float(amax) - 1.0) < 2.0 ** -23
+
+
+@pytest.mark.parametrize("mode", Q_MODES)
+def test_quant_reconstruction_within_half_an_e4m3_step(mode):
+    # |decode(q) * s - x| <= half a quantum: 2^-4 |x| for normal codes, half the
+    # subnormal step 2^-9 (times s) below 2^-6; plus the FP32 division's rounding.
+    rows, cols = 256, 384
+    x = synth.values_f32(12, 1, rows, cols, out_prob=0.01, out_factor=50.0).astype(np.float32)
+    q, s = oracle.quantize_e4m3(x, mode)
+    sel = s[_block_ids(rows, cols, mode)].astype(np.float64)
+    err = np.abs(oracle.e4m3_decode(q) * sel - x.astype(np.float64))
+    bound = 2.0 ** -4 * np.abs(x) * (1 + 2.0 ** -20) + 2.0 ** -10 * sel
+    assert (err <= bound).all()
+    # and it is not trivially loose: most elements sit well inside it
+    assert np.median(err / bound) < 0.6
+
+
+@pytest.mark.parametrize("mode", Q_MODES)
+def test_quant_matches_torch_division_and_float8_cast(mode):
+    # Given the scales, each code is torch's FP32 division followed by torch's
+    # float8_e4m3fn conversion; the scales are amax / 448 of numpy's max.
+    rows, cols = 200, 700
+    x = synth.values_f32(13, 1, rows, cols, out_prob=0.01, out_factor=50.0)
+    q, s = oracle.quantize_e4m3(x, mode)
+    ids = _block_ids(rows, cols, mode)
+    amax = np.zeros(_nblocks(rows, cols, mode), dtype=np.float32)
+    np.maximum.at(amax, ids.ravel(), np.abs(x).ravel())
+    assert np.array_equal(s, (torch.from_numpy(amax) / 448.0).numpy())
+    y = torch.from_numpy(x) / torch.from_numpy(s[ids])
+    ref = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+
+
+@pytest.mark.parametrize("mode,fn", [(oracle.Q_TENSOR, synth.e4m3_tensor),
+                                     (oracle.Q_ROW128, synth.e4m3_rowblock),
+                                     (oracle.Q_BLOCK128, synth.e4m3_block128)])
+def test_quant_matches_the_input_generators_quantiser(mode, fn):
+    x = synth.values_f32(14, 2, 384, 1152, out_prob=0.01, out_factor=50.0)
+    q, s = oracle.quantize_e4m3(x, mode, ldq=1168)
+    q2, s2 = fn(x, ld=1168)
+    assert np.array_equal(s, s2) and np.array_equal(q, q2)
+
+
+def test_quant_special_values():
+    # NaN entries are skipped by amax and stored as the canonical NaN 0x7F;
+    # -0 keeps its sign; an infinite amax gives scale inf, finite values -> +-0
+    # and inf/inf -> NaN.
+    x = np.array([[1.0, np.nan, -0.0, -448.0 * 4, 2.0 ** -40]], dtype=np.float32)
+    q, s = oracle.quantize_e4m3(x, oracle.Q_TENSOR)
+    assert s[0] == 4.0
+    assert q.tolist() == [[oracle.e4m3_encode(np.float32([0.25]))[0], 0x7F, 0x80, 0xFE, 0x00]]
+    xi = np.array([[1.0, -2.0, np.inf, -np.inf]], dtype=np.float32)
+    q, s = oracle.quantize_e4m3(xi, oracle.Q_TENSOR)
+    assert np.isinf(s[0]) and q.tolist() == [[0x00, 0x80, 0x7F, 0x7F]]
+    # amax so small that amax / 448 underflows to zero: scale 1, codes 0
+    xt = np.array([[2.0 ** -149, -(2.0 ** -149)]], dtype=np.float32)
+    q, s = oracle.quantize_e4m3(xt, oracle.Q_TENSOR)
+    assert s[0] == 1.0 and q.tolist() == [[0x00, 0x80]]
+    # empty inputs
+    q, s = oracle.quantize_e4m3(np.zeros((0, 5), np.float32), oracle.Q_TENSOR)
+    assert s.tolist() == [1.0] and q.shape == (0, 5)
+    q, s = oracle.quantize_e4m3(np.zeros((4, 0), np.float32), oracle.Q_ROW128)
+    assert s.size == 0
+
+
+@pytest.mark.parametrize("mode", Q_MODES)
+def test_quant_bf16_input_equals_fp32_input_of_the_same_values(mode):
+    bits = synth.bf16(15, 1, 130, 300, p1=3.0)
+    q1, s1 = oracle.quantize_e4m3(bits, mode)
+    q2, s2 = oracle.quantize_e4m3(oracle.bf16_decode(bits).astype(np.float32), mode)
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
