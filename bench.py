@@ -286,6 +286,65 @@ def time_graph(rot, steps, warmup):
 
 SECONDARY = ("fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64", "fp8_skinny_128")
 
+# The FP8 quantiser on the operands the FP8 workloads cast: (seed, tensor id,
+# rows, cols, granularity, outlier probability).  The values are the FP32
+# tensors synth.workloads quantises on the host for fp8_4096 (A, per tensor)
+# and fp8_skinny_M (A in 1 x 128 blocks, the 8192 x 8192 B in 128 x 128).
+QUANT = {
+    "quant_tensor_4096": (3, 1, 4096, 4096, "tensor", 0.0),
+    "quant_row128_128": (5, 1, 128, 8192, "row128", 0.01),
+    "quant_block128_8192": (5, 2, 8192, 8192, "block128", 0.01),
+}
+
+
+class QuantRotation:
+    """Device copies of one quantiser workload (FP32 X, codes, scales), with
+    one library call closure per copy, cycled so no call finds X in L2."""
+
+    def __init__(self, name):
+        import torch
+
+        import synth
+        import tensor_core_dense_gb300 as tcg
+        seed, tensor, rows, cols, gran, outl = QUANT[name]
+        x = synth.values_f32(seed, tensor, rows, cols, out_prob=outl, out_factor=50.0)
+        self.rows, self.cols, self.granularity = rows, cols, gran
+        mode = {"tensor": tcg.QUANT_TENSOR, "row128": tcg.QUANT_ROW128,
+                "block128": tcg.QUANT_BLOCK128}[gran]
+        nscale = tcg.quant_scale_count(rows, cols, mode)
+        self.input_bytes = x.nbytes
+        self.output_bytes = rows * cols + 4 * nscale
+        self.copies = rotation_count(self.input_bytes + self.output_bytes)
+        X0 = torch.from_numpy(x).cuda()
+        self.calls, self.tensors = [], []
+        for i in range(self.copies):
+            X = X0 if i == 0 else X0.clone()
+            Q = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+            S = torch.empty((nscale,), dtype=torch.float32, device="cuda")
+            self.tensors.append((X, Q, S))
+            self.calls.append(
+                lambda X=X, Q=Q, S=S: tcg.quantize_e4m3(X, Q, S, mode=mode,
+                                                        stream=torch.cuda.current_stream()))
+
+    def step(self, i):
+        self.calls[i % self.copies]()
+
+
+def quant_config(name, steps, warmup, hbm_peak):
+    """One quantiser workload: algorithmic bytes (X read once, codes and scales
+    written once) per call over the mean call time."""
+    rot = QuantRotation(name)
+    ms, launches, g = time_graph(rot, steps, warmup)
+    ms /= steps
+    nbytes = rot.input_bytes + rot.output_bytes
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out = {"workload": name, "rows": rot.rows, "cols": rot.cols,
+           "granularity": rot.granularity, "input": "f32", "us": round(ms * 1e3, 2),
+           "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4),
+           "kernels_per_call": launches // steps, "copies": rot.copies}
+    del rot, g
+    return out
+
 
 def secondary_configs(steps=50, warmup=5, names=SECONDARY):
     """The other workloads, timed the same way (context beside the main line)."""
@@ -294,6 +353,10 @@ def secondary_configs(steps=50, warmup=5, names=SECONDARY):
     import synth.workloads as W
     out = []
     for name in names:
+        if name in QUANT:
+            out.append(quant_config(name, steps, warmup, peaks()[1]))
+            torch.cuda.empty_cache()
+            continue
         w = W.make(name)
         rot = Rotation(w)
         ms, _, g = time_graph(rot, steps, warmup)
@@ -429,8 +492,10 @@ def run_ours(args):
     del rot, A, B, D
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_secondary:
-        line["other_configs"] = secondary_configs()
+        line["other_configs"] = secondary_configs(names=SECONDARY + tuple(QUANT))
         for o in line["other_configs"]:
+            if o["workload"] in QUANT:
+                continue
             if o["workload"].startswith("fp8"):
                 o["frac_of_fp8_peak"] = round(o["tflops"] / (peak_bf16 * FP8_OVER_BF16), 4)
             else:
@@ -509,7 +574,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the timed kernel from an ncu capture")
-    ap.add_argument("--only", choices=SECONDARY, default=None,
+    ap.add_argument("--only", choices=SECONDARY + tuple(QUANT), default=None,
                     help="time one secondary workload alone (for profiling); prints its line")
     args = ap.parse_args()
     if args.warmup < 3:

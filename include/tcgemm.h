@@ -139,6 +139,62 @@ tcg_status gemm_fp8_e4m3_block_noalloc(int64_t M, int64_t N, int64_t K, const vo
                                        int64_t ldc, void* D, int64_t ldd, tcg_out_dtype out_dtype,
                                        float alpha, float beta, tcg_stream stream);
 
+/* Element type of the quantiser's input. */
+typedef enum { TCG_IN_F32 = 0, TCG_IN_BF16 = 1 } tcg_in_dtype;
+
+/* Scale granularity of the quantiser, in the layouts gemm_fp8_e4m3 reads. */
+typedef enum {
+  /* one scale for the whole matrix: scale[0] */
+  TCG_QUANT_TENSOR = 0,
+  /* 1 x 128 blocks (row r, columns 128kb..128kb+127): scale[kb * rows + r];
+   * the A-operand layout of TCG_SCALE_BLOCK128 with rows = M */
+  TCG_QUANT_ROW128 = 1,
+  /* 128 x 128 blocks: scale[rb * ceil(cols/128) + kb]; the B-operand layout
+   * of TCG_SCALE_BLOCK128 with rows = N */
+  TCG_QUANT_BLOCK128 = 2
+} tcg_quant_mode;
+
+/*
+ * quantize_e4m3 -- FP8 E4M3 codes and FP32 dequantisation scales for a
+ * rows x cols matrix X, the step before gemm_fp8_e4m3.
+ *
+ * The recipe is FP8 scaling as "Tensor cores and low precision" gives it
+ * (FP8 paragraph): rescale so that the largest magnitude of a block sits at
+ * 448, E4M3's maximum normal value, then cast; the scale is removed after the
+ * product.  Scales per tensor, per row or per block ("Tensor Cores",
+ * "Precision: FP16, BF16, TF32, FP8").  For each block:
+ *     amax = max |x| over the block (NaN entries ignored)
+ *     s    = amax / 448 in FP32, correctly rounded; s = 1 if that is 0
+ *     Q    = E4M3(x / s): FP32 division, then round to nearest even,
+ *            saturating at +-448; a NaN quotient gives 0x7F
+ * and scale[...] = s, so that x is approximately decode(Q) * s.  A partial
+ * last block (rows or cols not a multiple of 128) uses its own amax.
+ *
+ * rows, cols   >= 0.  rows == 0 or cols == 0: with TCG_QUANT_TENSOR,
+ *              scale[0] = 1 is written; otherwise nothing is done.
+ * X, ldx       device pointer, element (r, c) at X[r * ldx + c], FP32 or BF16
+ *              (x_dtype); ldx >= cols; X 16-byte aligned, ldx * element size
+ *              a multiple of 16 bytes.
+ * Q, ldq       device pointer, one byte per element at Q[r * ldq + c];
+ *              ldq >= cols, Q 16-byte aligned, ldq a multiple of 16 (so Q can
+ *              be gemm_fp8_e4m3's A or B directly).  Bytes at columns >= cols
+ *              are not written.
+ * scale        device pointer, 4-byte aligned, FP32: 1 value (TENSOR),
+ *              rows * ceil(cols/128) (ROW128) or ceil(rows/128) *
+ *              ceil(cols/128) (BLOCK128) values.  With TCG_QUANT_TENSOR it
+ *              also serves as the running maximum while the call runs (it is
+ *              cleared on `stream`, then raised, then read).
+ * Errors       TCG_ERR_INVALID_ARG for negative sizes, NULL pointers or short
+ *              leading dimensions; TCG_ERR_ALIGNMENT as above;
+ *              TCG_ERR_UNSUPPORTED for an unknown x_dtype or mode, or rows or
+ *              cols >= 2^31.  Checked on the host before anything is enqueued.
+ * Work         ROW128 and BLOCK128: one kernel.  TENSOR: a 4-byte memset and
+ *              two kernels (block maxima, then codes).  Nothing is allocated.
+ */
+tcg_status quantize_e4m3(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                         tcg_in_dtype x_dtype, tcg_quant_mode mode, void* Q, int64_t ldq,
+                         float* scale, tcg_stream stream);
+
 /* A static, human-readable name for a status code. */
 const char* tcg_status_string(tcg_status status);
 

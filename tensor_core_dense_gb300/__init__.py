@@ -7,7 +7,8 @@ missing, importing the binding's entry points raises.
 
     D = alpha * A @ B.T + beta * C      (A: M x K, B: N x K, both K-major)
 
-The entry points keep the C names: ``gemm_bf16`` and ``gemm_fp8_e4m3``.
+The entry points keep the C names: ``gemm_bf16``, ``gemm_fp8_e4m3`` and the
+FP8 quantiser ``quantize_e4m3`` that produces the latter's codes and scales.
 """
 
 from __future__ import annotations
@@ -21,10 +22,12 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libtcgemm.so")
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(6)
 OUT_BF16, OUT_F32 = 0, 1
 SCALE_TENSOR, SCALE_BLOCK128 = 0, 1
+IN_F32, IN_BF16 = 0, 1
+QUANT_TENSOR, QUANT_ROW128, QUANT_BLOCK128 = 0, 1, 2
 
 # Every symbol include/tcgemm.h declares.
-EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8_e4m3_block_noalloc", "tcg_status_string",
-           "tcg_last_device_status", "tcg_launch_count")
+EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8_e4m3_block_noalloc", "quantize_e4m3",
+           "tcg_status_string", "tcg_last_device_status", "tcg_launch_count")
 
 _lib = None
 
@@ -51,6 +54,8 @@ def lib():
         L.gemm_fp8_e4m3.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, vp, i32, vp, i64, vp,
                                     i64, i32, f32, f32, vp]
         L.gemm_fp8_e4m3.restype = i32
+        L.quantize_e4m3.argtypes = [i64, i64, vp, i64, i32, i32, vp, i64, vp, vp]
+        L.quantize_e4m3.restype = i32
         L.tcg_status_string.argtypes = [i32]
         L.tcg_status_string.restype = ctypes.c_char_p
         L.tcg_last_device_status.argtypes = [vp]
@@ -95,6 +100,10 @@ def gemm_fp8_e4m3_raw(M, N, K, A, lda, B, ldb, a_scale, b_scale, mode, C, ldc, D
                       out_dtype, alpha, beta, stream) -> int:
     return int(lib().gemm_fp8_e4m3(M, N, K, A, lda, B, ldb, a_scale, b_scale, mode, C, ldc, D,
                                    ldd, out_dtype, float(alpha), float(beta), stream))
+
+
+def quantize_e4m3_raw(rows, cols, X, ldx, x_dtype, mode, Q, ldq, scale, stream) -> int:
+    return int(lib().quantize_e4m3(rows, cols, X, ldx, x_dtype, mode, Q, ldq, scale, stream))
 
 
 # --------------------------------------------------------------- tensor API
@@ -167,3 +176,36 @@ def gemm_fp8_e4m3(A, B, a_scale, b_scale, D, C=None, *, mode=SCALE_TENSOR, alpha
     if st != OK:
         raise TcgError(st, "gemm_fp8_e4m3")
     return D
+
+
+def quant_scale_count(rows, cols, mode):
+    """Number of FP32 scales quantize_e4m3 writes for a rows x cols input."""
+    kb, rb = -(-cols // 128), -(-rows // 128)
+    return {QUANT_TENSOR: 1, QUANT_ROW128: rows * kb, QUANT_BLOCK128: rb * kb}[mode]
+
+
+def quantize_e4m3(X, Q, scale, *, mode=QUANT_TENSOR, stream=None):
+    """FP8 E4M3 codes into Q (uint8 or float8_e4m3fn, rows x >=cols) and
+    dequantisation scales into `scale` (float32, quant_scale_count values) for
+    the float32 or bfloat16 matrix X (layouts in include/tcgemm.h)."""
+    import torch
+    if X.dtype == torch.float32:
+        x_dtype = IN_F32
+    elif X.dtype == torch.bfloat16:
+        x_dtype = IN_BF16
+    else:
+        raise ValueError("X must be float32 or bfloat16")
+    if Q.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError("Q must hold bytes")
+    if scale.dtype != torch.float32 or not scale.is_contiguous():
+        raise ValueError("scale must be a contiguous float32 tensor")
+    rows, cols = X.shape
+    if Q.shape[0] != rows or Q.shape[1] < cols:
+        raise ValueError("Q must be rows x (>= cols)")
+    if scale.numel() < quant_scale_count(rows, cols, mode):
+        raise ValueError("scale too small")
+    st = quantize_e4m3_raw(rows, cols, _ptr(X), _ld(X, "X"), x_dtype, mode, _ptr(Q), _ld(Q, "Q"),
+                           _ptr(scale), _stream_handle(stream))
+    if st != OK:
+        raise TcgError(st, "quantize_e4m3")
+    return Q, scale

@@ -1,4 +1,5 @@
-"""Compiles the CUDA library (csrc/*.cu) into _lib/libtcgemm.so for sm_103a.
+"""Compiles the CUDA library (csrc/*.cu) into _lib/libtcgemm.so for sm_103a
+(one nvcc per translation unit, in parallel, then one link).
 
 nvcc cross-compiles without a GPU.  The library links the CUDA runtime
 statically and reaches the driver's tensor-map encoder through
@@ -10,6 +11,7 @@ from __future__ import annotations
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
@@ -23,7 +25,7 @@ DEPS = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
     "--expt-relaxed-constexpr",
 ]
 
@@ -44,12 +46,22 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(LIB_DIR, exist_ok=True)
-    tmp = f"{LIB_PATH}.{os.getpid()}.tmp"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-I", CSRC,
-           *(extra or []), *SOURCES, "-o", tmp]
-    if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.check_call(cmd)
+    tag = f"{os.getpid()}.tmp"
+    objs = [os.path.join(LIB_DIR, os.path.basename(src)[:-3] + f".{tag}.o") for src in SOURCES]
+    cmds = [[nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-I", CSRC,
+             *(extra or []), "-c", src, "-o", obj] for src, obj in zip(SOURCES, objs)]
+    for c in cmds:
+        if verbose:
+            print(" ".join(c), file=sys.stderr)
+    # one nvcc per translation unit, in parallel, then one link
+    with ThreadPoolExecutor(len(cmds)) as ex:
+        for f in [ex.submit(subprocess.check_call, c) for c in cmds]:
+            f.result()
+    tmp = f"{LIB_PATH}.{tag}"
+    subprocess.check_call([nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
+                           *objs, "-o", tmp])
+    for o in objs:
+        os.remove(o)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

@@ -1,7 +1,8 @@
 // tcgemm.cu -- host side of the C ABI declared in include/tcgemm.h:
 // argument validation, TMA tensor-map encoding (cached), kernel selection and
-// launch.  The kernels themselves are in gemm_tn.cuh (large shapes, BF16 and
-// per-tensor FP8) and gemm_skinny.cuh (block-scaled FP8, M <= 128).
+// launch.  The kernels themselves are in gemm_tn2.cuh / gemm_tn.cuh (BF16 and
+// per-tensor FP8) and gemm_skinny.cuh (block-scaled FP8, M <= 128); the FP8
+// quantiser's are in quant.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -16,6 +17,7 @@
 #include "gemm_skinny.cuh"
 #include "gemm_tn.cuh"
 #include "gemm_tn2.cuh"
+#include "quant.cuh"
 #include "tcgemm.h"
 
 namespace tcg {
@@ -107,16 +109,18 @@ EncodeTiledFn get_encode_fn() {
 
 struct MapKey {
   uint64_t ptr, inner, rows, ld_bytes;
-  uint32_t dtype, box_inner, box_rows;
+  uint32_t dtype, box_inner, box_rows, swizzle;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && inner == o.inner && rows == o.rows && ld_bytes == o.ld_bytes &&
-           dtype == o.dtype && box_inner == o.box_inner && box_rows == o.box_rows;
+           dtype == o.dtype && box_inner == o.box_inner && box_rows == o.box_rows &&
+           swizzle == o.swizzle;
   }
 };
 struct MapKeyHash {
   size_t operator()(const MapKey& k) const {
     uint64_t h = 1469598103934665603ull;
-    const uint64_t v[7] = {k.ptr, k.inner, k.rows, k.ld_bytes, k.dtype, k.box_inner, k.box_rows};
+    const uint64_t v[8] = {k.ptr,   k.inner,     k.rows,     k.ld_bytes,
+                           k.dtype, k.box_inner, k.box_rows, k.swizzle};
     for (uint64_t x : v) h = (h ^ x) * 1099511628211ull;
     return (size_t)h;
   }
@@ -126,13 +130,14 @@ std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 constexpr size_t kMaxCachedMaps = 4096;
 
 // A 2-D row-major matrix (rows x inner elements, pitch ld_bytes) read in
-// boxes of box_rows x box_inner with 128-byte swizzling; out-of-range
-// elements read as zero.
+// boxes of box_rows x box_inner with 128-byte swizzling (or `swizzle`);
+// out-of-range elements read as zero.
 tcg_status tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, const void* ptr,
                       uint64_t inner, uint64_t rows, uint64_t ld_bytes, uint32_t box_inner,
-                      uint32_t box_rows) {
-  const MapKey key{(uint64_t)(uintptr_t)ptr, inner, rows, ld_bytes, (uint32_t)dtype, box_inner,
-                   box_rows};
+                      uint32_t box_rows,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+  const MapKey key{(uint64_t)(uintptr_t)ptr, inner,     rows,     ld_bytes,
+                   (uint32_t)dtype,          box_inner, box_rows, (uint32_t)swizzle};
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_maps.find(key);
@@ -150,7 +155,7 @@ tcg_status tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, const void* p
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return TCG_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_map_mu);
@@ -506,6 +511,72 @@ tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, cuda
   return launch_skinny_inst<128>(a, sa, sb, stream, dev, sms);
 }
 
+// ------------------------------------------------------------ quantiser
+
+template <int kIn, int kKind>
+tcg_status launch_quant_inst(const CUtensorMap& map, const QuantParams& p, int grid, int dev,
+                             cudaStream_t stream, bool pdl) {
+  auto* fn = &quant_e4m3_kernel<kIn, kKind>;
+  if (tcg_status s = ensure_smem(fn, kQSmemBytes, dev); s != TCG_OK) return s;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kQThreads, 1, 1);
+  cfg.dynamicSmemBytes = kQSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, fn, map, p) != cudaSuccess) return TCG_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+template <int kIn>
+tcg_status launch_quant(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                        tcg_quant_mode mode, void* Q, int64_t ldq, float* scale,
+                        cudaStream_t stream) {
+  int dev, sms;
+  if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+  const int64_t esize = kIn == 0 ? 4 : 2;
+  CUtensorMap map;
+  if (tcg_status s = tensor_map(&map,
+                                kIn == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                X, (uint64_t)cols, (uint64_t)rows, (uint64_t)(ldx * esize),
+                                kQBoxCols, kQBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+      s != TCG_OK)
+    return s;
+  QuantParams p{};
+  p.Q = static_cast<uint8_t*>(Q);
+  p.scale = scale;
+  p.ldq = ldq;
+  p.rows = (int32_t)rows;
+  p.cols = (int32_t)cols;
+  p.KB = (int32_t)((cols + 127) / 128);
+  const int64_t row_units = mode == TCG_QUANT_BLOCK128 ? (rows + 127) / 128 : (rows + 31) / 32;
+  const int64_t units = row_units * p.KB;
+  if (units > INT32_MAX) return TCG_ERR_UNSUPPORTED;
+  p.units = (int32_t)units;
+  const int grid = (int)(units < sms ? units : sms);
+  if (mode == TCG_QUANT_BLOCK128)
+    return launch_quant_inst<kIn, kQuantBlock>(map, p, grid, dev, stream, false);
+  if (mode == TCG_QUANT_ROW128)
+    return launch_quant_inst<kIn, kQuantRow>(map, p, grid, dev, stream, false);
+  // per tensor: clear the running maximum, fold the per-CTA maxima, encode.
+  // X is kept in L2 between the two passes when it fits comfortably.
+  int l2 = 0;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) l2 = 0;
+  p.keep_in_l2 = rows * ldx * esize <= (int64_t)l2 / 2 ? 1 : 0;
+  if (cudaMemsetAsync(scale, 0, sizeof(float), stream) != cudaSuccess) return TCG_ERR_CUDA;
+  if (tcg_status s = launch_quant_inst<kIn, kQuantAmax>(map, p, grid, dev, stream, false);
+      s != TCG_OK)
+    return s;
+  p.keep_in_l2 = 0;
+  return launch_quant_inst<kIn, kQuantEncode>(map, p, grid, dev, stream, true);
+}
+
 }  // namespace
 }  // namespace tcg
 
@@ -569,6 +640,33 @@ tcg_status tcg_last_device_status(tcg_stream stream) {
 }
 
 uint64_t tcg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+tcg_status quantize_e4m3(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                         tcg_in_dtype x_dtype, tcg_quant_mode mode, void* Q, int64_t ldq,
+                         float* scale, tcg_stream stream) {
+  if (x_dtype != TCG_IN_F32 && x_dtype != TCG_IN_BF16) return TCG_ERR_UNSUPPORTED;
+  if (mode != TCG_QUANT_TENSOR && mode != TCG_QUANT_ROW128 && mode != TCG_QUANT_BLOCK128)
+    return TCG_ERR_UNSUPPORTED;
+  if (rows < 0 || cols < 0) return TCG_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (rows == 0 || cols == 0) {
+    if (mode != TCG_QUANT_TENSOR) return TCG_OK;  // no blocks, no scales
+    if (!scale) return TCG_ERR_INVALID_ARG;
+    if ((uintptr_t)scale % 4 != 0) return TCG_ERR_ALIGNMENT;
+    quant_scale_one_kernel<<<1, 1, 0, st>>>(scale);  // the maximum of nothing is 0: scale 1
+    if (cudaGetLastError() != cudaSuccess) return TCG_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return TCG_OK;
+  }
+  if (!X || !Q || !scale || ldx < cols || ldq < cols) return TCG_ERR_INVALID_ARG;
+  const int64_t esize = x_dtype == TCG_IN_F32 ? 4 : 2;
+  if (!aligned16(X) || (ldx * esize) % 16 != 0 || !aligned16(Q) || ldq % 16 != 0 ||
+      (uintptr_t)scale % 4 != 0)
+    return TCG_ERR_ALIGNMENT;
+  if (rows > INT32_MAX || cols > INT32_MAX) return TCG_ERR_UNSUPPORTED;
+  return x_dtype == TCG_IN_F32 ? launch_quant<0>(rows, cols, X, ldx, mode, Q, ldq, scale, st)
+                               : launch_quant<1>(rows, cols, X, ldx, mode, Q, ldq, scale, st);
+}
 
 }  // extern "C"
 

@@ -84,3 +84,29 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(t, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         t.lib()
+
+
+X, Q, S = 0x10000, 0x20000, 0x30000   # never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("args,want", [
+    ((-1, 8, X, 8, 0, 0, Q, 16, S), 1),        # negative rows
+    ((8, 8, X, 4, 0, 0, Q, 16, S), 1),         # ldx < cols
+    ((8, 8, X, 8, 0, 0, Q, 4, S), 1),          # ldq < cols
+    ((8, 8, None, 8, 0, 0, Q, 16, S), 1),      # X NULL
+    ((8, 8, X, 8, 0, 1, None, 16, S), 1),      # Q NULL
+    ((8, 8, X, 8, 0, 2, Q, 16, None), 1),      # scale NULL
+    ((8, 8, X + 4, 8, 0, 0, Q, 16, S), 2),     # X misaligned
+    ((8, 6, X, 6, 0, 0, Q, 16, S), 2),         # ldx*4 not a multiple of 16
+    ((8, 4, X, 4, 1, 0, Q, 16, S), 2),         # BF16: ldx*2 not a multiple of 16
+    ((8, 8, X, 8, 0, 0, Q, 8, S), 2),          # ldq not a multiple of 16
+    ((8, 8, X, 8, 0, 0, Q + 1, 16, S), 2),     # Q misaligned
+    ((8, 8, X, 8, 0, 0, Q, 16, S + 2), 2),     # scale misaligned
+    ((8, 8, X, 8, 5, 0, Q, 16, S), 3),         # bad input dtype
+    ((8, 8, X, 8, 0, 7, Q, 16, S), 3),         # bad mode
+    ((0, 8, None, 0, 0, 1, None, 0, None), 0),  # empty, row blocks: no-op
+    ((8, 0, None, 0, 0, 2, None, 0, None), 0),  # empty, 128 x 128 blocks: no-op
+    ((0, 8, None, 0, 0, 0, None, 0, None), 1),  # empty per-tensor writes scale[0]: needs it
+])
+def test_quant_host_validation(tcg, args, want):
+    assert tcg.quantize_e4m3_raw(*args, None) == want
