@@ -26,6 +26,14 @@
 // writes D.  Only the first and the last piece of a CTA's range can be
 // partial tiles.
 //
+// When every tile is split into exactly two halves (kPair: N tiles * 2 <=
+// SMs < N tiles * 3, e.g. N = 8192), the two CTAs of a tile form a cluster
+// instead: each leaves its FP32 partial in its own shared memory, and after a
+// cluster barrier CTA r adds the two halves (lower K range first, so the
+// result is the same every run) for half of the tile's outputs, reading the
+// peer's partial over distributed shared memory -- no workspace, no atomics,
+// no global round trip at the end.
+//
 // Roles: warp 0 TMA producer (one lane), warp 1 TMEM allocator + MMA issuer
 // (one lane), then two (Mp <= 32) or four (Mp >= 64) epilogue warpgroups;
 // warpgroup h promotes its own slice of Mp/2 or Mp/4 columns of every
@@ -151,7 +159,7 @@ __device__ __forceinline__ void emit_four(const SkinnyParams& p, int m, int n, f
   }
 }
 
-template <int kMp>
+template <int kMp, bool kPair>
 __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     gemm_fp8_block_skinny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                  const __grid_constant__ CUtensorMap tmap_b,
@@ -392,7 +400,13 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
       // ---- this CTA's K range of tile nt is summed
       const int64_t tile_first = st - kb;
       const int kb_first = (int)((tile_first > s0 ? tile_first : s0) - tile_first);
-      if (kb_first == 0 && kb == KB - 1) {
+      if (kPair) {
+        // park the half-tile partial in this CTA's shared memory (every MMA
+        // and TMA copy of the range is complete: the stages are free)
+        float* part = reinterpret_cast<float*>(gbase);
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c) part[(col0 + c) * 128 + nloc] = acc[c];
+      } else if (kb_first == 0 && kb == KB - 1) {
         const int n = nt * 128 + nloc;
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) emit_one(p, col0 + c, n, acc[c]);
@@ -411,7 +425,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     }
     // ---- end of the range: count this CTA's partial tiles in, and finish
     // the tiles it is the last contributor to.
-    if (ok && npend > 0) {
+    if (!kPair && ok && npend > 0) {
       __threadfence();
       __syncwarp();
       if (lane == 0) mbar_arrive(seg_bar);
@@ -479,6 +493,28 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (kPair) {
+    cluster_sync_all();  // both halves' partials are in shared memory
+    if (warp >= 2 && !*abort_flag) {
+      // CTA r finishes float4 units [r*kUnits/2, (r+1)*kUnits/2) of the
+      // Mp x 128 tile (a unit is 4 consecutive n of one row m)
+      constexpr int kUnits = kMp * 32;
+      const uint32_t rank = cluster_ctarank();
+      const uint32_t local = smem_u32(gbase);
+      const uint32_t lo_half = map_shared_to_cta(local, 0);  // K blocks [0, KB/2)
+      const uint32_t hi_half = map_shared_to_cta(local, 1);
+      const int tnt = (int)(s0 / KB);
+      const int etid = (int)((warp - 2) * 32u + lane);
+      for (int u = (int)rank * (kUnits / 2) + etid; u < ((int)rank + 1) * (kUnits / 2);
+           u += kSkEpiThreads) {
+        const float4 a = ld_shared_cluster_v4(lo_half + 16u * (uint32_t)u);
+        const float4 b = ld_shared_cluster_v4(hi_half + 16u * (uint32_t)u);
+        emit_four(p, u >> 5, tnt * 128 + (u & 31) * 4,
+                  make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+      }
+    }
+    cluster_sync_all();  // the peer has finished reading this CTA's partial
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();

@@ -457,10 +457,11 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   // few partial sums to add; otherwise the steps are spread over all SMs and
   // every CTA gets at least ceil(KB/3) of them.  Either way at most kSkMaxSeg
   // (4) CTAs share a tile.
+  int64_t split = 0;
   {
     int64_t g;
     if (p.n_tiles < sms) {
-      int64_t split = sms / p.n_tiles;
+      split = sms / p.n_tiles;
       if (split > 3) split = 3;
       if (split > p.num_kb) split = p.num_kb;
       g = p.n_tiles * split;
@@ -471,11 +472,6 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
     }
     p.grid = (int32_t)(g < 1 ? 1 : g);
   }
-  // Segments per tile: a tile of num_kb steps meets at most
-  // ceil(num_kb / min_range) + 1 ranges, min_range = floor(T / grid).
-  const int64_t min_range = T / p.grid;
-  p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);
-  if (p.max_seg > p.grid) p.max_seg = p.grid;
   p.a_scale = sa;
   p.b_scale = sb;
   p.C = a.beta != 0.0f ? a.C : nullptr;
@@ -486,6 +482,22 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   p.beta = a.beta;
   p.out_f32 = a.out == TCG_OUT_F32;
   p.has_c = a.beta != 0.0f;
+  if (split == 2) {
+    // two halves per tile: a cluster of the two CTAs joins them in shared
+    // memory (no workspace)
+    auto* fn = &gemm_fp8_block_skinny_kernel<kMp, true>;
+    if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
+    if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 2, ma, mb, p) !=
+        cudaSuccess)
+      return TCG_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+  }
+  // Segments per tile: a tile of num_kb steps meets at most
+  // ceil(num_kb / min_range) + 1 ranges, min_range = floor(T / grid).
+  const int64_t min_range = T / p.grid;
+  p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);
+  if (p.max_seg > p.grid) p.max_seg = p.grid;
   if (p.num_kb > 1) {  // a tile may be split over CTAs: needs the workspace
     const size_t partial_bytes = (size_t)p.n_tiles * p.max_seg * kMp * 128 * sizeof(float);
     if (tcg_status s = get_workspace(dev, (size_t)p.n_tiles * sizeof(unsigned int),
@@ -493,7 +505,7 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
         s != TCG_OK)
       return s;
   }
-  auto* fn = &gemm_fp8_block_skinny_kernel<kMp>;
+  auto* fn = &gemm_fp8_block_skinny_kernel<kMp, false>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
   if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 1, ma, mb, p) !=
       cudaSuccess)
@@ -786,7 +798,7 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
   p.beta = a.beta;
   p.out_f32 = a.out == TCG_OUT_F32;
   p.has_c = a.beta != 0.0f;
-  auto* fn = &gemm_fp8_block_skinny_kernel<kMp>;
+  auto* fn = &gemm_fp8_block_skinny_kernel<kMp, false>;
   {  // raise the shared-memory limit once per device (no host-side table)
     static bool raised[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(g_noalloc_mu);

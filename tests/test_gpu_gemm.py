@@ -216,7 +216,10 @@ def test_fp8_tensor_scales_bit_exact():
 # ------------------------------------------------------- FP8 block, skinny M
 
 SKINNY = [(1, 128, 128), (16, 300, 200), (17, 1024, 4096), (64, 2000, 1000),
-          (100, 1024, 4096), (128, 256, 8192), (128, 4096, 1024)]
+          (100, 1024, 4096), (128, 256, 8192), (128, 4096, 1024),
+          # N tiles in [SMs/3, SMs/2]: each tile's K range is cut in two and the
+          # halves are joined by a cluster of two CTAs (odd and even K blocks)
+          (5, 7000, 1000), (33, 6528, 384), (100, 8100, 256), (128, 9728, 1152)]
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY)
@@ -226,7 +229,8 @@ def test_fp8_block_skinny_shapes(M, N, K, out, beta):
     check_full(w, run(w))
 
 
-@pytest.mark.parametrize("M,N,K", [(5, 260, 300), (64, 1024, 4096), (128, 2048, 2048)])
+@pytest.mark.parametrize("M,N,K", [(5, 260, 300), (64, 1024, 4096), (128, 2048, 2048),
+                                   (20, 8192, 640)])
 def test_fp8_block_scale_indexing_bit_exact(M, N, K):
     """Power-of-two block scales that depend on (row, K block) and (N block,
     K block) with small-integer codes: every misplaced scale changes bits."""
@@ -248,8 +252,9 @@ def test_fp8_block_scale_indexing_bit_exact(M, N, K):
     assert np.array_equal(d_to_host(run(w)).astype(np.float64), v)
 
 
-def test_fp8_block_skinny_deterministic():
-    w = fp8_case(64, 4096, 4096, seed=11, mode="block", out="f32", outliers=0.01)
+@pytest.mark.parametrize("M,N", [(64, 4096), (16, 8192)])
+def test_fp8_block_skinny_deterministic(M, N):
+    w = fp8_case(M, N, 4096, seed=11, mode="block", out="f32", outliers=0.01)
     d1 = d_to_host(run(w))
     d2 = d_to_host(run(w))
     assert np.array_equal(d1.view(np.uint32), d2.view(np.uint32))
