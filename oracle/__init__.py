@@ -13,7 +13,8 @@ with gcc and marshals numpy arrays.  Sources and readings:
   Instructions, Swizzling and FP8, Measured", Step 1), with B stored N x K,
   K contiguous (same page, Step 2);
 * BF16 = 1/8/7 bits ("Tensor Cores", "Precision: FP16, BF16, TF32, FP8");
-* E4M3 = 1/4/3 bits, no infinity, max normal 448, hence bias 7 ("Tensor cores
+* E4M3 = 1/4/3 bits, no infinity, max normal 448, hence bias 7; E5M2 = 1/5/2
+  bits, IEEE special values, max normal 57,344, hence bias 15 ("Tensor cores
   and low precision", the FP8 paragraph);
 * FP8 scale factors applied after the product ("Tensor cores and low
   precision", the scaling paragraph), per tensor or per 128-wide K block;
@@ -47,6 +48,7 @@ IN_BF16, IN_E4M3 = 0, 1
 Q_TENSOR, Q_ROW128, Q_BLOCK128 = 0, 1, 2
 SCALE_NONE, SCALE_TENSOR, SCALE_BLOCK128 = 0, 1, 2
 C_BF16, C_F32 = 0, 1
+FP8_E4M3, FP8_E5M2 = 0, 1
 
 
 class _Args(ctypes.Structure):
@@ -68,6 +70,8 @@ class _Args(ctypes.Structure):
         ("pad_", ctypes.c_int32),
         ("alpha", ctypes.c_double),
         ("beta", ctypes.c_double),
+        ("a_fp8", ctypes.c_int32),
+        ("b_fp8", ctypes.c_int32),
     ]
 
 
@@ -96,7 +100,7 @@ def _load():
         lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
         for name in ("orc_bf16_decode_array", "orc_bf16_encode_array",
                      "orc_e4m3_decode_array", "orc_e4m3_encode_array",
-                     "orc_cast_bf16_array"):
+                     "orc_e5m2_decode_array", "orc_cast_bf16_array"):
             getattr(lib, name).argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             getattr(lib, name).restype = None
         lib.orc_gemm_tiles.argtypes = [ctypes.POINTER(_Args), ctypes.c_int64, ctypes.c_void_p,
@@ -136,6 +140,11 @@ def e4m3_decode(bits) -> np.ndarray:
     return _elementwise("orc_e4m3_decode_array", bits, np.uint8, np.float64)
 
 
+def e5m2_decode(bits) -> np.ndarray:
+    """E5M2 bytes -> float64 values (+-inf for S.11111.00, NaN for other S.11111.xx)."""
+    return _elementwise("orc_e5m2_decode_array", bits, np.uint8, np.float64)
+
+
 def e4m3_encode(x) -> np.ndarray:
     """float32 values -> E4M3 bytes, nearest even, saturating at +-448."""
     return _elementwise("orc_e4m3_encode_array", x, np.float32, np.uint8)
@@ -155,10 +164,11 @@ def default_threads() -> int:
 
 def gemm(M, N, K, A, lda, B, ldb, *, in_type=IN_BF16, scale_mode=SCALE_NONE,
          a_scale=None, b_scale=None, C=None, ldc=0, c_type=C_F32, alpha=1.0, beta=0.0,
-         tiles=None, nthreads=None):
+         tiles=None, nthreads=None, a_fp8=FP8_E4M3, b_fp8=FP8_E4M3):
     """Reference values and error bounds for D = alpha*A*B + beta*C.
 
-    A: flat uint16 (BF16) or uint8 (E4M3) array, element (i, k) at A[i*lda + k].
+    A: flat uint16 (BF16) or uint8 (FP8) array, element (i, k) at A[i*lda + k];
+       with in_type=IN_E4M3 the bytes are E4M3 or E5M2 per a_fp8 / b_fp8.
     B: same dtype, element (k, j) at B[j*ldb + k] (N x K, K contiguous).
     C: flat uint16 (c_type=C_BF16) or float32 (C_F32) array, (i, j) at C[i*ldc + j];
        not read when beta == 0.
@@ -195,7 +205,7 @@ def gemm(M, N, K, A, lda, B, ldb, *, in_type=IN_BF16, scale_mode=SCALE_NONE,
         a_scale = b_scale = None
     args = _Args(M, N, K, in_type, scale_mode, _ptr(A), lda, _ptr(B), ldb,
                  _ptr(a_scale), _ptr(b_scale), _ptr(C), ldc, c_type, 0,
-                 float(alpha), float(beta))
+                 float(alpha), float(beta), int(a_fp8), int(b_fp8))
     whole = tiles is None
     if whole:
         tiles = [(0, 0, M, N)]

@@ -30,12 +30,19 @@
  *    1.75 * 2^8 is the largest finite value with exponent field 15 and
  *    mantissa 110, so the exponent bias is 7 and only mantissa 111 at
  *    exponent 15 is NaN.
+ *  - E5M2 is 1 / 5 / 2 bits with IEEE 754 behaviour for the special values
+ *    and maximum normal 57,344 (same paragraph).  57,344 = 1.75 * 2^15 is the
+ *    largest finite value with exponent field 30 (31 is kept for infinity and
+ *    NaN, as in IEEE 754), so the bias is 15.  Either operand of an FP8 GEMM
+ *    may be E4M3 or E5M2.
  *
  * Accumulation is in FP64.  BF16 x BF16 products are exact in FP64.  For
  * E4M3 the raw code products q_a * q_b (at most 8 significant bits, exponents
  * 2^-18 .. 2^17) are summed per 128-wide K block, which is exact, and only
  * then multiplied by the block's FP64 scale product s_a * s_b (exact, 24+24
- * bits).  The sum of |a_ik * b_kj| is returned beside each value as the
+ * bits).  With E5M2 operands (exponents 2^-16 .. 2^15) a block sum can span
+ * more than 53 bits and is exact only up to FP64 rounding, at most
+ * 128 * 2^-53 of the block's sum of |products|.  The sum of |a_ik * b_kj| is returned beside each value as the
  * error bound the tolerances are stated against.
  *
  * The scale layouts for the 128-block mode (the pages name block scaling but
@@ -61,6 +68,8 @@
 #define ORC_SCALE_BLOCK128 2
 #define ORC_C_BF16 0
 #define ORC_C_F32 1
+#define ORC_FP8_E4M3 0
+#define ORC_FP8_E5M2 1
 
 /* ------------------------------------------------------------------ codecs */
 
@@ -140,6 +149,27 @@ uint8_t orc_e4m3_encode(float f) {
   return (uint8_t)(sign | (uint8_t)(efield << 3) | (uint8_t)(r - 8));
 }
 
+/* E5M2 bits -> value.  S.EEEEE.MM, bias 15; exponent field 0 is subnormal
+ * (M/4 * 2^-14); exponent field 31 is infinity (M = 0) or NaN (M != 0). */
+double orc_e5m2_decode(uint8_t b) {
+  int s = (b >> 7) & 1;
+  int e = (b >> 2) & 31;
+  int m = b & 3;
+  double mag;
+  if (e == 31) {
+    if (m != 0) return NAN;
+    mag = INFINITY;
+  } else {
+    mag = (e == 0) ? ldexp((double)m, -16)             /* (m/4) * 2^-14 */
+                   : ldexp((double)(4 + m), e - 17);   /* (1+m/4) * 2^(e-15) */
+  }
+  return s ? -mag : mag;
+}
+
+void orc_e5m2_decode_array(const uint8_t* in, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e5m2_decode(in[i]);
+}
+
 void orc_bf16_decode_array(const uint16_t* in, int64_t n, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_decode(in[i]);
 }
@@ -176,11 +206,13 @@ typedef struct {
   int32_t c_type; /* ORC_C_BF16 / ORC_C_F32 */
   int32_t pad_;
   double alpha, beta;
+  int32_t a_fp8, b_fp8; /* FP8 inputs: ORC_FP8_E4M3 / ORC_FP8_E5M2 per operand */
 } orc_gemm_args;
 
-static double dec_in(const orc_gemm_args* g, const void* base, int64_t idx) {
+static double dec_in(const orc_gemm_args* g, const void* base, int64_t idx, int32_t fp8) {
   if (g->in_type == ORC_IN_BF16) return orc_bf16_decode(((const uint16_t*)base)[idx]);
-  return orc_e4m3_decode(((const uint8_t*)base)[idx]);
+  uint8_t b = ((const uint8_t*)base)[idx];
+  return fp8 == ORC_FP8_E5M2 ? orc_e5m2_decode(b) : orc_e4m3_decode(b);
 }
 
 static double dec_c(const orc_gemm_args* g, int64_t i, int64_t j) {
@@ -240,9 +272,11 @@ static int gemm_tile(const orc_gemm_args* g, int64_t i0, int64_t j0, int64_t mi,
     return -1;
   }
   for (int64_t r = 0; r < mi; ++r)
-    for (int64_t k = 0; k < K; ++k) arows[r * K + k] = dec_in(g, g->A, (i0 + r) * g->lda + k);
+    for (int64_t k = 0; k < K; ++k)
+      arows[r * K + k] = dec_in(g, g->A, (i0 + r) * g->lda + k, g->a_fp8);
   for (int64_t c = 0; c < nj; ++c)
-    for (int64_t k = 0; k < K; ++k) brows[c * K + k] = dec_in(g, g->B, (j0 + c) * g->ldb + k);
+    for (int64_t k = 0; k < K; ++k)
+      brows[c * K + k] = dec_in(g, g->B, (j0 + c) * g->ldb + k, g->b_fp8);
   for (int64_t r = 0; r < mi; ++r)
     for (int64_t c = 0; c < nj; ++c)
       gemm_one(g, arows + r * K, brows + c * K, i0 + r, j0 + c, &v[r * nj + c], &bound[r * nj + c]);

@@ -72,7 +72,7 @@ def _load():
                      "synth_quant_e4m3_block128"):
             getattr(lib, name).argtypes = [vp, i64, i64, i64, vp, vp]
             getattr(lib, name).restype = None
-        for name in ("synth_to_bf16_array", "synth_to_e4m3_array"):
+        for name in ("synth_to_bf16_array", "synth_to_e4m3_array", "synth_to_e5m2_array"):
             getattr(lib, name).argtypes = [vp, i64, vp]
             getattr(lib, name).restype = None
         _lib = lib
@@ -151,6 +151,14 @@ def to_e4m3(x) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     out = np.empty(x.shape, dtype=np.uint8)
     _load().synth_to_e4m3_array(x.ctypes.data, x.size, out.ctypes.data)
+    return out
+
+
+def to_e5m2(x) -> np.ndarray:
+    """float32 -> E5M2 bytes, nearest even, saturating at +-57344."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().synth_to_e5m2_array(x.ctypes.data, x.size, out.ctypes.data)
     return out
 
 

@@ -108,6 +108,31 @@ static uint8_t to_e4m3(float f) {
   return (uint8_t)(s | (uint8_t)(e4 << 3) | (uint8_t)m3);
 }
 
+/* E5M2, nearest-even, saturating at +-57344 (like the E4M3 encoder).
+ * Normals: round the FP32 pattern at bit 21 and re-bias the exponent
+ * (127 -> 15).  Below 2^-14: the grid is k * 2^-16 (scale by 2^16, exact,
+ * and rint).  57344 = 1.75 * 2^15; halfway to 2^16 (61440) and above
+ * saturate. */
+static uint8_t to_e5m2(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  uint8_t s = (uint8_t)((u >> 24) & 0x80u);
+  uint32_t a = u & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return (uint8_t)(s | 0x7Fu);
+  float m;
+  memcpy(&m, &a, 4);
+  if (m < 0x1.0p-14f) {
+    int k = (int)rintf(m * 65536.0f); /* 0..4; 4 is the smallest normal 0x04 */
+    return (uint8_t)(s | (uint8_t)k);
+  }
+  if (m >= 61440.0f) return (uint8_t)(s | 0x7Bu);
+  uint32_t r = (a + 0xFFFFFu + ((a >> 21) & 1u)) >> 21; /* exponent:8 | mantissa:2 */
+  uint32_t e8 = r >> 2, m2 = r & 3u;
+  uint32_t e5 = e8 - 127u + 15u;
+  if (e5 > 30u) return (uint8_t)(s | 0x7Bu);
+  return (uint8_t)(s | (uint8_t)(e5 << 2) | (uint8_t)m2);
+}
+
 /* ---- threaded row loops ------------------------------------------------- */
 
 typedef struct {
@@ -242,4 +267,7 @@ void synth_to_bf16_array(const float* x, int64_t n, uint16_t* out) {
 }
 void synth_to_e4m3_array(const float* x, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = to_e4m3(x[i]);
+}
+void synth_to_e5m2_array(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = to_e5m2(x[i]);
 }

@@ -48,6 +48,47 @@ def test_e4m3_facts_from_the_pages():
     assert int(facts["e4m3_exponent_bits"]) + int(facts["e4m3_mantissa_bits"]) + 1 == 8
 
 
+def test_e5m2_facts_from_the_pages():
+    facts = {r[0]: r[1] for r in _golden("e4m3_format.txt")}
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.e5m2_decode(codes)
+    finite = vals[np.isfinite(vals)]
+    assert finite.max() == float(facts["e5m2_max_normal"]) == 57344.0 == -finite.min()
+    # IEEE specials kept: infinities at S.11111.00, NaN at S.11111.{01,10,11}
+    assert int(facts["e5m2_has_infinity"]) == 1
+    assert vals[0x7C] == np.inf and vals[0xFC] == -np.inf
+    assert np.isnan(vals).sum() == 6 and all(np.isnan(vals[c]) for c in (0x7D, 0x7E, 0x7F))
+    assert int(facts["e5m2_exponent_bits"]) + int(facts["e5m2_mantissa_bits"]) + 1 == 8
+    # bias 15: 1.0 is 0.01111.00, the smallest subnormal 2^-16
+    assert vals[0x3C] == 1.0 and vals[0x01] == 2.0 ** -16 and vals[0x04] == 2.0 ** -14
+    assert (np.diff(vals[:0x7C]) > 0).all()
+
+
+def test_e5m2_decode_matches_torch_float8_e5m2_for_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e5m2).to(torch.float64).numpy()
+    got = oracle.e5m2_decode(codes)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    m = ~np.isnan(ref)
+    assert np.array_equal(ref[m], got[m]) and np.array_equal(np.signbit(ref[m]), np.signbit(got[m]))
+
+
+def test_e5m2_generator_encoder_against_torch_and_decode():
+    # the input generator's E5M2 encoder (test inputs only): round trip of every
+    # finite code, nearest-even on 4M random values (torch's cast agrees inside
+    # the finite range), saturation at +-57344 where torch overflows to inf
+    codes = np.array([c for c in range(256) if np.isfinite(oracle.e5m2_decode(
+        np.array([c], np.uint8)))[0]], dtype=np.uint8)
+    assert np.array_equal(synth.to_e5m2(oracle.e5m2_decode(codes).astype(np.float32)), codes)
+    x = (np.random.default_rng(3).standard_normal(1 << 22) *
+         np.exp2(np.random.default_rng(4).integers(-20, 16, 1 << 22))).astype(np.float32)
+    x = x[np.abs(x) < 61440.0]
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(synth.to_e5m2(x), ref)
+    big = np.array([57344.0, 60000.0, 61440.0, 1e9, np.inf], np.float32)
+    assert (synth.to_e5m2(big) == 0x7B).all() and (synth.to_e5m2(-big) == 0xFB).all()
+
+
 def test_e4m3_decode_matches_torch_float8_for_all_codes():
     codes = np.arange(256, dtype=np.uint8)
     ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
@@ -243,6 +284,47 @@ def test_fp8_tensor_scale_exact():
     b = _frac_rows(oracle.e4m3_decode(qb.ravel()), N, K, K)
     ex = _exact_gemm(M, N, K, a, b, sa=sa, sb=sb)
     assert all(Fraction(v[i, j]) == ex[i][j] for i in range(M) for j in range(N))
+
+
+@pytest.mark.parametrize("a_fp8,b_fp8", [(1, 1), (0, 1), (1, 0)])
+@pytest.mark.parametrize("mode", ["tensor", "block"])
+def test_e5m2_operands_exact_rational(a_fp8, b_fp8, mode):
+    # E5M2 (and mixed E4M3 x E5M2) operands against exact rational sums:
+    # within FP64 rounding of the block sums (E5M2's wider exponent range can
+    # take a 128-term sum past 53 bits), scales applied per block
+    M, N, K = 3, 140, 260
+    KB, NB = (K + 127) // 128, (N + 127) // 128
+    rng = np.random.default_rng(10 + 3 * a_fp8 + b_fp8)
+
+    def codes(fmt, rows):
+        q = rng.integers(0, 256, size=(rows, K)).astype(np.uint8)
+        if fmt == 1:
+            q[(q & 0x7C) == 0x7C] = 0x3C   # no inf/NaN codes
+        else:
+            q[(q & 0x7F) == 0x7F] = 0x38
+        return q
+    qa, qb = codes(a_fp8, M), codes(b_fp8, N)
+    dec = {0: oracle.e4m3_decode, 1: oracle.e5m2_decode}
+    if mode == "tensor":
+        sa, sb, sm = np.array([2.0 ** -7], np.float32), np.array([3.0], np.float32), \
+            oracle.SCALE_TENSOR
+    else:
+        sa = np.exp2(rng.integers(-4, 4, KB * M)).astype(np.float32)
+        sb = (np.exp2(rng.integers(-4, 4, NB * KB)) * 1.5).astype(np.float32)
+        sm = oracle.SCALE_BLOCK128
+    v, bound = oracle.gemm(M, N, K, qa, K, qb, K, in_type=oracle.IN_E4M3, scale_mode=sm,
+                           a_scale=sa, b_scale=sb, a_fp8=a_fp8, b_fp8=b_fp8)
+    a = _frac_rows(dec[a_fp8](qa.ravel()), M, K, K)
+    b = _frac_rows(dec[b_fp8](qb.ravel()), N, K, K)
+    ex = _exact_gemm(M, N, K, a, b, sa=sa, sb=sb, block=(mode == "block"))
+    for i in range(M):
+        for j in range(N):
+            assert abs(Fraction(v[i, j]) - ex[i][j]) <= Fraction(K + 2, 2 ** 52) * Fraction(
+                bound[i, j]), (i, j)
+    # and the format matters: decoding as E4M3 gives another result
+    v2, _ = oracle.gemm(M, N, K, qa, K, qb, K, in_type=oracle.IN_E4M3, scale_mode=sm,
+                        a_scale=sa, b_scale=sb)
+    assert not np.array_equal(v, v2)
 
 
 # ------------------------------------------------------------ closed forms
