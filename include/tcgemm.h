@@ -107,6 +107,26 @@ tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t
                          tcg_scale_mode mode, const void* C, int64_t ldc, void* D, int64_t ldd,
                          tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream);
 
+/* The two 8-bit floating-point encodings ("Tensor cores and low precision",
+ * FP8 paragraph): E4M3 (1/4/3 bits, bias 7, no infinity, maximum 448) and
+ * E5M2 (1/5/2 bits, bias 15, IEEE infinities and NaNs, maximum 57,344). */
+typedef enum { TCG_FP8_E4M3 = 0, TCG_FP8_E5M2 = 1 } tcg_fp8_format;
+
+/*
+ * gemm_fp8 -- gemm_fp8_e4m3 with the encoding of each operand given
+ * separately: E4M3 x E4M3, E5M2 x E5M2, or mixed (E4M3 activations or weights
+ * against E5M2 gradients, the pages' suggested split between the formats).
+ * Arguments, layouts, scale modes, alignment and numerics are those of
+ * gemm_fp8_e4m3; codes must be finite (no E5M2 infinities or NaNs).  An
+ * unknown format returns TCG_ERR_UNSUPPORTED.  gemm_fp8_e4m3(...) is
+ * gemm_fp8 with a_format = b_format = TCG_FP8_E4M3.
+ */
+tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                    tcg_fp8_format a_format, const void* B, int64_t ldb, tcg_fp8_format b_format,
+                    const float* a_scale, const float* b_scale, tcg_scale_mode mode,
+                    const void* C, int64_t ldc, void* D, int64_t ldd, tcg_out_dtype out_dtype,
+                    float alpha, float beta, tcg_stream stream);
+
 /*
  * gemm_fp8_e4m3_block_noalloc -- the TCG_SCALE_BLOCK128 case of gemm_fp8_e4m3
  * (M <= 128) without any device allocation.  The pages have no counterpart

@@ -47,6 +47,8 @@ class Workload:
     a_scale: np.ndarray = None
     b_scale: np.ndarray = None
     meta: dict = field(default_factory=dict)
+    a_fp8: int = 0        # FP8 encodings of A and B: 0 = E4M3, 1 = E5M2
+    b_fp8: int = 0
 
     @property
     def flops(self) -> int:

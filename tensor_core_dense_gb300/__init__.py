@@ -7,8 +7,9 @@ missing, importing the binding's entry points raises.
 
     D = alpha * A @ B.T + beta * C      (A: M x K, B: N x K, both K-major)
 
-The entry points keep the C names: ``gemm_bf16``, ``gemm_fp8_e4m3`` and the
-FP8 quantiser ``quantize_e4m3`` that produces the latter's codes and scales.
+The entry points keep the C names: ``gemm_bf16``, ``gemm_fp8_e4m3``, ``gemm_fp8``
+(E4M3 / E5M2 per operand) and the FP8 quantiser ``quantize_e4m3`` that
+produces the FP8 GEMM's codes and scales.
 """
 
 from __future__ import annotations
@@ -23,11 +24,12 @@ OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = ran
 OUT_BF16, OUT_F32 = 0, 1
 SCALE_TENSOR, SCALE_BLOCK128 = 0, 1
 IN_F32, IN_BF16 = 0, 1
+FP8_E4M3, FP8_E5M2 = 0, 1
 QUANT_TENSOR, QUANT_ROW128, QUANT_BLOCK128 = 0, 1, 2
 
 # Every symbol include/tcgemm.h declares.
-EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8_e4m3_block_noalloc", "quantize_e4m3",
-           "tcg_status_string", "tcg_last_device_status", "tcg_launch_count")
+EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8", "gemm_fp8_e4m3_block_noalloc",
+           "quantize_e4m3", "tcg_status_string", "tcg_last_device_status", "tcg_launch_count")
 
 _lib = None
 
@@ -54,6 +56,9 @@ def lib():
         L.gemm_fp8_e4m3.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, vp, i32, vp, i64, vp,
                                     i64, i32, f32, f32, vp]
         L.gemm_fp8_e4m3.restype = i32
+        L.gemm_fp8.argtypes = [i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, vp, i32, vp, i64,
+                               vp, i64, i32, f32, f32, vp]
+        L.gemm_fp8.restype = i32
         L.quantize_e4m3.argtypes = [i64, i64, vp, i64, i32, i32, vp, i64, vp, vp]
         L.quantize_e4m3.restype = i32
         L.tcg_status_string.argtypes = [i32]
@@ -100,6 +105,13 @@ def gemm_fp8_e4m3_raw(M, N, K, A, lda, B, ldb, a_scale, b_scale, mode, C, ldc, D
                       out_dtype, alpha, beta, stream) -> int:
     return int(lib().gemm_fp8_e4m3(M, N, K, A, lda, B, ldb, a_scale, b_scale, mode, C, ldc, D,
                                    ldd, out_dtype, float(alpha), float(beta), stream))
+
+
+def gemm_fp8_raw(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale, b_scale, mode, C, ldc,
+                 D, ldd, out_dtype, alpha, beta, stream) -> int:
+    return int(lib().gemm_fp8(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale, b_scale,
+                              mode, C, ldc, D, ldd, out_dtype, float(alpha), float(beta),
+                              stream))
 
 
 def quantize_e4m3_raw(rows, cols, X, ldx, x_dtype, mode, Q, ldq, scale, stream) -> int:
@@ -150,6 +162,45 @@ def gemm_bf16(A, B, D, C=None, *, alpha=1.0, beta=0.0, stream=None):
                        alpha, beta if C is not None else 0.0, _stream_handle(stream))
     if st != OK:
         raise TcgError(st, "gemm_bf16")
+    return D
+
+
+def _fp8_format(t, given, name):
+    import torch
+    if t.dtype == torch.float8_e5m2:
+        fmt = FP8_E5M2
+    elif t.dtype == torch.float8_e4m3fn:
+        fmt = FP8_E4M3
+    elif t.dtype == torch.uint8:
+        fmt = FP8_E4M3 if given is None else given
+    else:
+        raise ValueError(f"{name} must hold FP8 bytes")
+    if given is not None and given != fmt:
+        raise ValueError(f"{name}: format {given} does not match dtype {t.dtype}")
+    return fmt
+
+
+def gemm_fp8(A, B, a_scale, b_scale, D, C=None, *, mode=SCALE_TENSOR, a_format=None,
+             b_format=None, alpha=1.0, beta=0.0, stream=None):
+    """D = alpha * (sa.A) @ (sb.B).T + beta * C with FP8 A, B: float8_e4m3fn /
+    float8_e5m2 tensors, or uint8 with a_format / b_format (default E4M3), and
+    FP32 scale tensors on the device (layouts in include/tcgemm.h)."""
+    import torch
+    af, bf = _fp8_format(A, a_format, "A"), _fp8_format(B, b_format, "B")
+    if a_scale.dtype != torch.float32 or b_scale.dtype != torch.float32:
+        raise ValueError("scales must be float32")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    if C is not None and (tuple(C.shape) != (M, N) or C.dtype != D.dtype):
+        raise ValueError("C must match D")
+    st = gemm_fp8_raw(M, N, K, _ptr(A), _ld(A, "A"), af, _ptr(B), _ld(B, "B"), bf, _ptr(a_scale),
+                      _ptr(b_scale), mode, _ptr(C), _ld(C, "C") if C is not None else 0, _ptr(D),
+                      _ld(D, "D"), _out_dtype(D), alpha, beta if C is not None else 0.0,
+                      _stream_handle(stream))
+    if st != OK:
+        raise TcgError(st, "gemm_fp8")
     return D
 
 

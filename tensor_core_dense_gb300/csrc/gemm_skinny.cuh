@@ -92,6 +92,8 @@ struct SkinnyParams {
   int64_t ldd;
   float alpha, beta;
   int32_t out_f32, has_c;
+  uint32_t fp8_fmt;  // UMMA A (= B, the weights) / UMMA B (= A) format fields
+  int32_t pad_;
   float* ws;               // [n_tiles][max_seg][Mp][128] partial sums
   unsigned int* counters;  // [n_tiles], zero between calls
 };
@@ -170,7 +172,8 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
   constexpr int kSkNumAcc = Cfg::kNumAcc;
   constexpr int kSkEpiThreads = Cfg::kEpiThreads;
   constexpr uint32_t kEpiWarps = Cfg::kEpiWarps;
-  constexpr uint32_t kIdesc = make_idesc(0, 0, 128, kMp);  // E4M3 x E4M3 -> F32, M=128, N=Mp
+  // FP8 x FP8 -> F32, M=128, N=Mp; the operand formats come from p.fp8_fmt
+  const uint32_t kIdesc = make_idesc(0, 0, 128, kMp) | p.fp8_fmt;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);

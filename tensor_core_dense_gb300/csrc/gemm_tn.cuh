@@ -76,7 +76,8 @@ struct GemmParams {
   // dp_end), then sub-tile units u = b + j*gridDim.x (u < (num_tiles -
   // dp_end) * split) of the remaining tiles, each split into `split` pieces
   // along N.
-  int32_t dp_waves, dp_end, split, pad_;
+  int32_t dp_waves, dp_end, split;
+  uint32_t fp8_fmt;  // FP8: A/B format fields of the instruction descriptor
   const void* C;
   int64_t ldc;
   void* D;
@@ -376,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_phase(tempty_bar(acc), aph ^ 1u, abort_flag, 2)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        const uint32_t idesc = w.split == 1 ? kIdesc256 : w.split == 2 ? kIdesc128 : kIdesc64;
+        const uint32_t idesc = (w.split == 1 ? kIdesc256 : w.split == 2 ? kIdesc128 : kIdesc64) |
+                               (kIn == 1 ? p.fp8_fmt : 0u);
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
           if (!wait_phase(full_bar(s), ph, abort_flag, 3)) {

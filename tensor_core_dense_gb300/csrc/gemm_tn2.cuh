@@ -41,7 +41,8 @@ constexpr uint32_t kP2SmemBytes = kP2Stages * kP2StageBytes + 1024 + 1024;
 struct Gemm2Params {
   int32_t M, N, K;
   int32_t tiles_m, tiles_n, num_kb, num_tiles;  // tiles are 256 x 256
-  int32_t dp_waves, dp_end, split, pad_;        // as GemmParams; split 1 or 2
+  int32_t dp_waves, dp_end, split;              // as GemmParams; split 1 or 2
+  uint32_t fp8_fmt;                             // as GemmParams
   const void* C;
   int64_t ldc;
   void* D;
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!free_ok) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        const uint32_t idesc = w.split == 1 ? kIdesc256 : kIdesc128;
+        const uint32_t idesc = (w.split == 1 ? kIdesc256 : kIdesc128) | (kIn == 1 ? p.fp8_fmt : 0u);
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
           if (!wait_phase(full_bar(s), ph, abort_flag, 0x23)) {

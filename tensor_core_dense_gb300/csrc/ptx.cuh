@@ -204,8 +204,9 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor for kind::f16 / kind::f8f6f4 with an FP32
-// accumulator and both operands K-major.  fmt: BF16 = 1 (kind::f16),
-// E4M3 = 0 (kind::f8f6f4).  N in steps of 16 (M = 128), M in steps of 16.
+// accumulator and both operands K-major.  fmt: BF16 = 1 (kind::f16); E4M3 =
+// 0, E5M2 = 1 (kind::f8f6f4, where A and B may differ).  N in steps of 16
+// (M = 128), M in steps of 16.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t M,
                                                   uint32_t N) {
   return (1u << 4)              // D format: F32

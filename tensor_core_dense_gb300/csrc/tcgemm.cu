@@ -215,7 +215,13 @@ struct Common {
   void* D;
   int out;  // tcg_out_dtype
   float alpha, beta;
+  int a_fp8 = 0, b_fp8 = 0;  // tcg_fp8_format of A and B (FP8 entry points)
 };
+
+// FP8 operand formats as the instruction descriptor's A and B fields.
+uint32_t fp8_fmt_bits(int umma_a, int umma_b) {
+  return ((uint32_t)umma_a << 7) | ((uint32_t)umma_b << 10);
+}
 
 // Checks shared by both entry points; in_bytes = bytes per A/B element.
 tcg_status validate(const Common& a, int in_bytes) {
@@ -356,6 +362,7 @@ tcg_status launch_tn2(const Common& a, const float* a_scale, const float* b_scal
   p.alpha = a.alpha;
   p.beta = a.beta;
   p.a_scale = a_scale;
+  p.fp8_fmt = fp8_fmt_bits(a.a_fp8, a.b_fp8);
   p.b_scale = b_scale;
   const int grid = 2 * clusters;
   const bool has_c = a.beta != 0.0f;
@@ -402,6 +409,7 @@ tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale
   p.alpha = a.alpha;
   p.beta = a.beta;
   p.a_scale = a_scale;
+  p.fp8_fmt = fp8_fmt_bits(a.a_fp8, a.b_fp8);
   p.b_scale = b_scale;
   // Schedule: whole waves of tiles run one tile per CTA; the tiles left for a
   // last partial wave (or all tiles, when there are fewer than SMs) are cut
@@ -473,6 +481,7 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
     p.grid = (int32_t)(g < 1 ? 1 : g);
   }
   p.a_scale = sa;
+  p.fp8_fmt = fp8_fmt_bits(a.b_fp8, a.a_fp8);  // swap-AB: UMMA A is B
   p.b_scale = sb;
   p.C = a.beta != 0.0f ? a.C : nullptr;
   p.ldc = a.ldc;
@@ -607,12 +616,18 @@ tcg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
   return launch_tn<0>(a, nullptr, nullptr, st);
 }
 
-tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                         const void* B, int64_t ldb, const float* a_scale, const float* b_scale,
-                         tcg_scale_mode mode, const void* C, int64_t ldc, void* D, int64_t ldd,
-                         tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream) {
-  const Common a{M, N, K, A, B, C, lda, ldb, ldc, ldd, D, (int)out_dtype, alpha, beta};
+tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                    tcg_fp8_format a_format, const void* B, int64_t ldb, tcg_fp8_format b_format,
+                    const float* a_scale, const float* b_scale, tcg_scale_mode mode,
+                    const void* C, int64_t ldc, void* D, int64_t ldd, tcg_out_dtype out_dtype,
+                    float alpha, float beta, tcg_stream stream) {
+  Common a{M, N, K, A, B, C, lda, ldb, ldc, ldd, D, (int)out_dtype, alpha, beta};
   if (mode != TCG_SCALE_TENSOR && mode != TCG_SCALE_BLOCK128) return TCG_ERR_UNSUPPORTED;
+  if ((a_format != TCG_FP8_E4M3 && a_format != TCG_FP8_E5M2) ||
+      (b_format != TCG_FP8_E4M3 && b_format != TCG_FP8_E5M2))
+    return TCG_ERR_UNSUPPORTED;
+  a.a_fp8 = (int)a_format;
+  a.b_fp8 = (int)b_format;
   if (tcg_status s = validate(a, 1); s != TCG_OK) return s;
   if (M == 0 || N == 0) return TCG_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -621,6 +636,14 @@ tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t
   if (mode == TCG_SCALE_TENSOR) return launch_tn<1>(a, a_scale, b_scale, st);
   if (M > 128) return TCG_ERR_UNSUPPORTED;
   return launch_skinny(a, a_scale, b_scale, st);
+}
+
+tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, const float* a_scale, const float* b_scale,
+                         tcg_scale_mode mode, const void* C, int64_t ldc, void* D, int64_t ldd,
+                         tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream) {
+  return gemm_fp8(M, N, K, A, lda, TCG_FP8_E4M3, B, ldb, TCG_FP8_E4M3, a_scale, b_scale, mode, C,
+                  ldc, D, ldd, out_dtype, alpha, beta, stream);
 }
 
 const char* tcg_status_string(tcg_status status) {

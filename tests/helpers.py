@@ -73,7 +73,8 @@ def oracle_for(w, tiles=None, C_override=None, nthreads=None):
     return oracle.gemm(w.M, w.N, w.K, w.A, w.lda, w.B, w.ldb, in_type=in_type, scale_mode=mode,
                        a_scale=w.a_scale, b_scale=w.b_scale, C=C,
                        ldc=(C.shape[1] if C is not None else 0), c_type=c_type, alpha=w.alpha,
-                       beta=w.beta, tiles=tiles, nthreads=nthreads)
+                       beta=w.beta, tiles=tiles, nthreads=nthreads, a_fp8=w.a_fp8,
+                       b_fp8=w.b_fp8)
 
 
 def c_values(C):
@@ -122,8 +123,14 @@ def run(w, out=None, C=None, alpha=None, beta=None, stream=None, D=None):
         tcg.gemm_bf16(A[:, :w.K], B[:, :w.K], D, Cd, alpha=alpha, beta=beta, stream=stream)
     else:
         mode = tcg.SCALE_TENSOR if w.kind == "fp8_tensor" else tcg.SCALE_BLOCK128
-        tcg.gemm_fp8_e4m3(A[:, :w.K], B[:, :w.K], to_device(w.a_scale), to_device(w.b_scale), D,
-                          Cd, mode=mode, alpha=alpha, beta=beta, stream=stream)
+        if w.a_fp8 == 0 and w.b_fp8 == 0:
+            tcg.gemm_fp8_e4m3(A[:, :w.K], B[:, :w.K], to_device(w.a_scale),
+                              to_device(w.b_scale), D, Cd, mode=mode, alpha=alpha, beta=beta,
+                              stream=stream)
+        else:
+            tcg.gemm_fp8(A[:, :w.K], B[:, :w.K], to_device(w.a_scale), to_device(w.b_scale), D,
+                         Cd, mode=mode, a_format=w.a_fp8, b_format=w.b_fp8, alpha=alpha,
+                         beta=beta, stream=stream)
     return D
 
 

@@ -313,3 +313,97 @@ def test_launch_counter_and_status():
     torch.cuda.synchronize()
     assert tcg.launch_count() == n0 + 1
     assert tcg.last_device_status() == tcg.OK
+
+
+# --------------------------------------------------------- E5M2 operands
+
+FMTS = [(1, 1), (0, 1), (1, 0)]  # (A, B): 0 = E4M3, 1 = E5M2
+
+
+def fp8_fmt_case(M, N, K, seed, mode, a_fmt, b_fmt, out="f32", beta=0.0):
+    """FP8 operands in the given encodings: N(0,1) values with 1% outliers x50,
+    cast with a scale that puts the largest magnitudes near the format's top
+    (448 or 57344), per tensor or in the 1 x 128 / 128 x 128 block layouts."""
+    w = W.Workload(f"fp8_{a_fmt}{b_fmt}_{mode}_{M}x{N}x{K}", M, N, K,
+                   "fp8_tensor" if mode == "tensor" else "fp8_block", out, beta=beta)
+    w.a_fp8, w.b_fp8 = a_fmt, b_fmt
+    ldk = _pad(K, 16)
+    KB, MB, NB = (K + 127) // 128, 1, (N + 127) // 128
+
+    def cast(x, fmt, scale_el):
+        q = np.zeros((x.shape[0], ldk), np.uint8)
+        y = (x / scale_el).astype(np.float32)
+        q[:, :K] = synth.to_e5m2(y) if fmt == 1 else synth.to_e4m3(y)
+        return q
+
+    top = {0: 448.0, 1: 57344.0}
+    xa = synth.values_f32(seed, 1, M, K, out_prob=0.01, out_factor=50.0)
+    xb = synth.values_f32(seed, 2, N, K, out_prob=0.01, out_factor=50.0)
+    if mode == "tensor":
+        sa = np.array([np.abs(xa).max() / top[a_fmt]], np.float32)
+        sb = np.array([np.abs(xb).max() / top[b_fmt]], np.float32)
+        w.A, w.B = cast(xa, a_fmt, sa[0]), cast(xb, b_fmt, sb[0])
+    else:
+        kb = np.arange(K) // 128
+        sa2 = np.stack([np.abs(xa[:, kb == j]).max(1) for j in range(KB)]) / top[a_fmt]  # KB x M
+        sb2 = np.array([[np.abs(xb[n * 128:(n + 1) * 128][:, kb == j]).max() for j in range(KB)]
+                        for n in range(NB)]) / top[b_fmt]                                     # NB x KB
+        sa2, sb2 = np.maximum(sa2, 1e-30).astype(np.float32), np.maximum(sb2, 1e-30).astype(np.float32)
+        w.A = cast(xa, a_fmt, sa2.T[:, kb])
+        w.B = cast(xb, b_fmt, np.repeat(sb2, 128, axis=0)[:N][:, kb])
+        sa, sb = sa2.ravel(), sb2.ravel()
+    w.a_scale, w.b_scale = sa, sb
+    if beta != 0.0:
+        if out == "bf16":
+            w.C = synth.bf16(seed, 3, M, N, ld=_pad(N, 8))
+        else:
+            w.C = np.zeros((M, _pad(N, 4)), np.float32)
+            w.C[:, :N] = synth.values_f32(seed, 3, M, N)
+    return w
+
+
+@pytest.mark.parametrize("kernel", ["1cta", "2cta"])
+@pytest.mark.parametrize("a_fmt,b_fmt", FMTS)
+@pytest.mark.parametrize("M,N,K,out,beta", [(200, 300, 520, "f32", 0.0),
+                                            (640, 512, 1024, "bf16", 1.0)])
+def test_fp8_e5m2_tensor_scaled(monkeypatch, kernel, a_fmt, b_fmt, M, N, K, out, beta):
+    monkeypatch.setenv("TCG_KERNEL", kernel)
+    w = fp8_fmt_case(M, N, K, seed=M + K + 7 * a_fmt + b_fmt, mode="tensor", a_fmt=a_fmt,
+                     b_fmt=b_fmt, out=out, beta=beta)
+    check_full(w, run(w))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", FMTS)
+@pytest.mark.parametrize("M,N,K", [(16, 1000, 1024), (100, 8192, 512), (128, 384, 2048)])
+def test_fp8_e5m2_block_scaled_skinny(a_fmt, b_fmt, M, N, K):
+    w = fp8_fmt_case(M, N, K, seed=M + N + K + 7 * a_fmt + b_fmt, mode="block", a_fmt=a_fmt,
+                     b_fmt=b_fmt)
+    check_full(w, run(w))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", FMTS)
+def test_fp8_e5m2_small_integers_bit_exact(a_fmt, b_fmt):
+    """Small integers (exact in both encodings) with power-of-two scales: the
+    FP32 accumulation is exact, so a format mix-up changes bits."""
+    M, N, K = 130, 260, 384
+    rng = np.random.default_rng(5 + a_fmt + 2 * b_fmt)
+    ints = np.array([-6, -5, -3, -2, -1, 0, 1, 2, 3, 5, 6], np.float32)
+    ldk = _pad(K, 16)
+    a = np.zeros((M, ldk), np.float32)
+    b = np.zeros((N, ldk), np.float32)
+    a[:, :K] = rng.choice(ints, size=(M, K))
+    b[:, :K] = rng.choice(ints, size=(N, K))
+    enc = {0: synth.to_e4m3, 1: synth.to_e5m2}
+    w = W.Workload("fp8_int_exact", M, N, K, "fp8_tensor", "f32")
+    w.a_fp8, w.b_fp8 = a_fmt, b_fmt
+    w.A, w.B = enc[a_fmt](a), enc[b_fmt](b)
+    w.a_scale = np.array([2.0 ** -2], np.float32)
+    w.b_scale = np.array([2.0 ** 3], np.float32)
+    v, _ = oracle_for(w)
+    for kern in ("1cta", "2cta"):
+        import os
+        os.environ["TCG_KERNEL"] = kern
+        try:
+            assert np.array_equal(d_to_host(run(w)).astype(np.float64), v), kern
+        finally:
+            del os.environ["TCG_KERNEL"]
