@@ -41,12 +41,13 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def kernel_source_sha():
-    """sha256 over the CUDA sources, to tell whether a stored ncu figure is current."""
+def kernel_source_sha(files=None):
+    """sha256 over CUDA sources (all of csrc/, or the named files), to tell
+    whether a stored ncu figure is still current."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_core_dense_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files or os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
@@ -60,10 +61,12 @@ def stored_traffic(summary="gemm_tn2_bf16_4096.md"):
         fields = {}
         with open(path) as f:
             for line in f:
-                if ":" in line and line.strip().startswith(("source_sha256", "traffic_bytes")):
+                if ":" in line and line.strip().startswith(
+                        ("source_sha256", "source_files", "traffic_bytes")):
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip().strip("`")
-        if fields.get("source_sha256") != kernel_source_sha():
+        files = fields.get("source_files", "").split() or None
+        if fields.get("source_sha256") != kernel_source_sha(files):
             return None
         return int(fields["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -77,6 +80,15 @@ def peaks():
         return float(p["bf16_tflops"]), float(p.get("hbm_gbs", 6800.0)), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+def sustained_peak():
+    """The measured bf16 rate of a seconds-long GEMM loop under the power cap."""
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -481,6 +493,8 @@ def run_ours(args):
                      "peak": peak_bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_bf16, 4),
                      "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "frac_of_sustained": (round(achieved / sustained_peak(), 4)
+                                           if sustained_peak() else None),
                      "kernel": "gemm_tn2_kernel<bf16,bf16 out> (CTA pair)",
                      "traffic": stored_traffic() if args.traffic is None else args.traffic},
         "gpu_launches": launches,
@@ -567,7 +581,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads")
