@@ -226,6 +226,18 @@ const char* tcg_status_string(tcg_status status);
  */
 tcg_status tcg_last_device_status(tcg_stream stream);
 
+/*
+ * tcg_debug_timeout_probe -- exercises the failure path every kernel's waits
+ * share, for tests.  Enqueues one CTA whose only work is a bounded wait on an
+ * mbarrier that nothing signals: after the library's wait limit (2 s) it
+ * records TCG_ERR_TIMEOUT in the device status word and returns (no trap, no
+ * fault; the context stays usable).  tcg_last_device_status(stream) then
+ * reports TCG_ERR_TIMEOUT once.  The pages have no counterpart: it tests the
+ * bounded waits the build adds because a spinning wait on a shared GPU must
+ * end.
+ */
+tcg_status tcg_debug_timeout_probe(tcg_stream stream);
+
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t tcg_launch_count(void);
 

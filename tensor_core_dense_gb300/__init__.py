@@ -29,7 +29,8 @@ QUANT_TENSOR, QUANT_ROW128, QUANT_BLOCK128 = 0, 1, 2
 
 # Every symbol include/tcgemm.h declares.
 EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8", "gemm_fp8_e4m3_block_noalloc",
-           "quantize_e4m3", "tcg_status_string", "tcg_last_device_status", "tcg_launch_count")
+           "quantize_e4m3", "tcg_status_string", "tcg_last_device_status", "tcg_launch_count",
+           "tcg_debug_timeout_probe")
 
 _lib = None
 
@@ -65,6 +66,8 @@ def lib():
         L.tcg_status_string.restype = ctypes.c_char_p
         L.tcg_last_device_status.argtypes = [vp]
         L.tcg_last_device_status.restype = i32
+        L.tcg_debug_timeout_probe.argtypes = [vp]
+        L.tcg_debug_timeout_probe.restype = i32
         L.tcg_launch_count.argtypes = []
         L.tcg_launch_count.restype = ctypes.c_uint64
         _lib = L

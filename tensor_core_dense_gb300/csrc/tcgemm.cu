@@ -46,6 +46,24 @@ __global__ void scale_c_kernel(int64_t M, int64_t N, const void* C, int64_t ldc,
   }
 }
 
+// ------------------------------------------------------ timeout probe
+
+// One CTA waits on an mbarrier that nothing arrives on, with the library's
+// bounded wait: it must give up after kWaitLimitNs, record TCG_ERR_TIMEOUT
+// in the status word and return, leaving the context usable.
+__global__ void wait_timeout_probe_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)wait_phase(smem_u32(&bar), 0, &abort_flag, 0x7E);
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------- devices
 
 struct DeviceInfo {
@@ -675,6 +693,13 @@ tcg_status tcg_last_device_status(tcg_stream stream) {
 }
 
 uint64_t tcg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+tcg_status tcg_debug_timeout_probe(tcg_stream stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+  if (cudaGetLastError() != cudaSuccess) return TCG_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return TCG_OK;
+}
 
 tcg_status quantize_e4m3(int64_t rows, int64_t cols, const void* X, int64_t ldx,
                          tcg_in_dtype x_dtype, tcg_quant_mode mode, void* Q, int64_t ldq,

@@ -407,3 +407,35 @@ def test_fp8_e5m2_small_integers_bit_exact(a_fmt, b_fmt):
             assert np.array_equal(d_to_host(run(w)).astype(np.float64), v), kern
         finally:
             del os.environ["TCG_KERNEL"]
+
+
+# ------------------------------------------------------------- guard bands
+
+@pytest.mark.parametrize("case", ["bf16_1cta", "bf16_2cta", "fp8_tensor", "fp8_block",
+                                  "fp8_block_pair"])
+def test_output_guard_bands_untouched(monkeypatch, case):
+    """D is a view into a larger buffer filled with a sentinel: the kernels
+    write exactly the M x N view (no row, column or padding outside it)."""
+    if case.startswith("bf16"):
+        monkeypatch.setenv("TCG_KERNEL", case.split("_")[1])
+        w = bf16_case(300, 200, 96, seed=51, out="f32")
+    elif case == "fp8_tensor":
+        w = fp8_case(300, 260, 128, seed=52, mode="tensor", out="bf16")
+    elif case == "fp8_block":
+        w = fp8_case(20, 300, 256, seed=53, mode="block", out="f32")
+    else:
+        w = fp8_case(100, 8192, 256, seed=54, mode="block", out="bf16")
+    dt = torch.float32 if w.out == "f32" else torch.bfloat16
+    step = 4 if dt == torch.float32 else 8
+    ldd = _pad(w.N, step) + 2 * step
+    big = torch.full((w.M + 2, ldd), float("nan"), dtype=dt, device="cuda")
+    sentinel = big.clone()
+    D = big[1:w.M + 1, step:step + w.N]
+    run(w, D=D)
+    torch.cuda.synchronize()
+    mask = torch.ones_like(big, dtype=torch.bool)
+    mask[1:w.M + 1, step:step + w.N] = False
+    outside = big[mask].view(torch.int16 if dt == torch.bfloat16 else torch.int32)
+    expect = sentinel[mask].view(torch.int16 if dt == torch.bfloat16 else torch.int32)
+    assert torch.equal(outside, expect), "a kernel wrote outside D"
+    check_full(w, D)
