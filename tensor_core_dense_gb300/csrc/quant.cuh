@@ -12,12 +12,12 @@
 //
 // The work is a stream over X (read once, twice for one scale per tensor)
 // and Q (written once): HBM-bound, no tensor cores.  A persistent CTA per SM:
-// one producer lane moves 32-row x 128-column boxes of X into a 128 KB
+// one producer lane moves 64-row x 128-column boxes of X into a 192 KB
 // shared-memory ring with TMA (out-of-range elements arrive as zeros, which no
 // block maximum can exceed), and sixteen consumer warps take each box out of
-// shared memory (warp w: rows 2w, 2w+1; lane l: columns 4l..4l+3), so HBM
+// shared memory (warp w: rows 4w..4w+3; lane l: columns 4l..4l+3), so HBM
 // stays busy while they reduce, divide and store.  Units of work:
-//   BLOCK128  a 128 x 128 block = 4 boxes; CTA-wide maximum, then codes
+//   BLOCK128  a 128 x 128 block = 2 boxes; CTA-wide maximum, then codes
 //   ROW128    one box; each row is its own 1 x 128 block (warp-wide maximum)
 //   TENSOR    two launches over boxes: the maxima, folded into scale[0] with
 //             an integer atomicMax (bit patterns of non-negative floats order
@@ -48,10 +48,11 @@ namespace tcg {
 
 constexpr int kQConsumerWarps = 16;
 constexpr int kQThreads = 32 * (kQConsumerWarps + 1);  // + one producer warp
-constexpr int kQBoxRows = 32;
+constexpr int kQBoxRows = 64;
 constexpr int kQBoxCols = 128;
-constexpr int kQRowsPerWarp = kQBoxRows / kQConsumerWarps;  // 2
-constexpr uint32_t kQRingBytes = 128u * 1024u;
+constexpr int kQRowsPerWarp = kQBoxRows / kQConsumerWarps;  // 4
+constexpr int kQBoxesPerBlock = 128 / kQBoxRows;             // boxes of one 128 x 128 block
+constexpr uint32_t kQRingBytes = 192u * 1024u;
 constexpr uint32_t kQSmemBytes = kQRingBytes + 1024u /*barriers, slots*/ + 1024u /*align*/;
 
 enum QuantKind { kQuantBlock = 0, kQuantAmax = 1, kQuantEncode = 2, kQuantRow = 3 };
@@ -62,12 +63,12 @@ struct QuantParams {
   int64_t ldq;
   int32_t rows, cols;
   int32_t KB;     // column blocks: ceil(cols / 128)
-  int32_t units;  // BLOCK: ceil(rows/128) * KB; otherwise ceil(rows/32) * KB
+  int32_t units;  // BLOCK: ceil(rows/128) * KB; otherwise ceil(rows/kQBoxRows) * KB
   int32_t keep_in_l2;  // TENSOR maxima pass: load X with an evict-last policy
   int32_t pad_;
 };
 
-// Unit u -> first row, first column and number of 32-row boxes.
+// Unit u -> first row, first column and number of boxes.
 template <int kKind>
 __device__ __forceinline__ void quant_unit(const QuantParams& p, int u, int& r0, int& c0,
                                            int& nbox) {
@@ -75,7 +76,7 @@ __device__ __forceinline__ void quant_unit(const QuantParams& p, int u, int& r0,
   c0 = kb * kQBoxCols;
   if (kKind == kQuantBlock) {
     r0 = (u / p.KB) * 128;
-    nbox = min(4, (p.rows - r0 + kQBoxRows - 1) / kQBoxRows);
+    nbox = min(kQBoxesPerBlock, (p.rows - r0 + kQBoxRows - 1) / kQBoxRows);
   } else {
     r0 = (u / p.KB) * kQBoxRows;
     nbox = 1;
@@ -126,8 +127,9 @@ __device__ __forceinline__ float quant_quotient(float x, const QuantDiv& d) {
 }
 
 // Four codes E4M3(x / s), packed little-endian (first element in the low
-// byte).  cvt.rn.satfinite rounds to nearest even and clamps finite overflow
-// to +-448; NaN bytes are made the canonical 0x7F.
+// byte).  cvt.rn.satfinite rounds to nearest even, clamps finite overflow and
+// infinities to +-448 and turns a NaN of either sign into the canonical 0x7F
+// (checked on GB300 for +-NaN, +-inf, +-0, subnormal ties and 464).
 __device__ __forceinline__ uint32_t quant_encode4(const float (&v)[4], const QuantDiv& d) {
   float y[4];
   if (d.exact) {
@@ -140,11 +142,7 @@ __device__ __forceinline__ uint32_t quant_encode4(const float (&v)[4], const Qua
   uint16_t lo, hi;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(y[1]), "f"(y[0]));
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(y[3]), "f"(y[2]));
-  uint32_t w = (uint32_t)lo | ((uint32_t)hi << 16);
-  // a byte 0xFF (negative NaN; 0x7F/0xFF are E4M3's only NaNs) loses its sign
-  // bit: (low seven bits + 1) reaches bit 7 only for 0x7F, no carry between bytes
-  w ^= ((w & 0x7F7F7F7Fu) + 0x01010101u) & w & 0x80808080u;
-  return w;
+  return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
 // Stores one row's four codes at columns c..c+3 (those < cols); `full`
@@ -274,10 +272,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       quant_unit<kKind>(p, u, r0, c0, nbox);
       const int c = c0 + 4 * lane;
       const bool full = r0 + nbox * kQBoxRows <= p.rows && c0 + kQBoxCols <= p.cols &&
-                        (kKind != kQuantBlock || nbox == 4);
+                        (kKind != kQuantBlock || nbox == kQBoxesPerBlock);
       if (kKind == kQuantBlock) {
-        float v[4 * kQRowsPerWarp][4];
-        for (int j = 0; j < 4; ++j) {
+        float v[kQBoxesPerBlock * kQRowsPerWarp][4];
+        for (int j = 0; j < kQBoxesPerBlock; ++j) {
           if (j < nbox) {
             const int s = (int)(it % S);
             if (!quant_warp_wait(full_bar(s), (it / S) & 1u, abort_flag, 0x42)) {
@@ -301,7 +299,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (!ok) break;
         float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4 * kQRowsPerWarp; ++i) m = fmaxf(m, abs_max4(v[i]));
+        for (int i = 0; i < kQBoxesPerBlock * kQRowsPerWarp; ++i) m = fmaxf(m, abs_max4(v[i]));
         m = warp_max(m);
         const uint32_t par = nunit & 1u;
         if (lane == 0) {
@@ -318,7 +316,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const QuantDiv d = quant_div(quant_scale_of(m));
         if (threadIdx.x == 0) p.scale[u] = d.s;  // u = rb * KB + kb
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < kQBoxesPerBlock; ++j)
 #pragma unroll
           for (int i = 0; i < kQRowsPerWarp; ++i)
             quant_store4(p, r0 + j * kQBoxRows + warp * kQRowsPerWarp + i, c,

@@ -594,7 +594,8 @@ tcg_status launch_quant(int64_t rows, int64_t cols, const void* X, int64_t ldx,
   p.rows = (int32_t)rows;
   p.cols = (int32_t)cols;
   p.KB = (int32_t)((cols + 127) / 128);
-  const int64_t row_units = mode == TCG_QUANT_BLOCK128 ? (rows + 127) / 128 : (rows + 31) / 32;
+  const int64_t row_units =
+      mode == TCG_QUANT_BLOCK128 ? (rows + 127) / 128 : (rows + kQBoxRows - 1) / kQBoxRows;
   const int64_t units = row_units * p.KB;
   if (units > INT32_MAX) return TCG_ERR_UNSUPPORTED;
   p.units = (int32_t)units;

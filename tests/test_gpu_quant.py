@@ -119,6 +119,9 @@ def test_special_values(mode):
     x[200, 300] = np.inf
     x[201, 301] = -np.inf
     x[250, 130:140] = np.nan
+    # NaNs of both signs and with payloads must all come out as 0x7F
+    x[251, 131:135] = np.array([0xFFC00000, 0x7F800001, 0xFF812345, 0x7FFFFFFF],
+                               np.uint32).view(np.float32)
     x[140, 140:200] = -1e-30                             # rounds to -0
     x[160:170, 260:270] = rng.choice([1e-38, -3e-39, 5e-40], size=(10, 10))
     check(x.astype(np.float32), mode)
