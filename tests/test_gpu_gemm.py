@@ -439,3 +439,39 @@ def test_output_guard_bands_untouched(monkeypatch, case):
     expect = sentinel[mask].view(torch.int16 if dt == torch.bfloat16 else torch.int32)
     assert torch.equal(outside, expect), "a kernel wrote outside D"
     check_full(w, D)
+
+
+# ------------------------------------------------------------ maximum sizes
+
+def test_bf16_output_beyond_2_31_elements():
+    """A 65,536 x 40,960 output (2.7e9 elements, 5.4 GB of BF16): row and
+    column offsets past 2^31 elements, checked on the corner tiles."""
+    M, N, K = 65536, 40960, 16
+    w = W.Workload("bf16_huge_mn", M, N, K, "bf16", "bf16")
+    w.A = synth.bf16(61, 1, M, K)
+    w.B = synth.bf16(61, 2, N, K)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    run(w, D=D)
+    torch.cuda.synchronize()
+    tiles = [(0, 0, 128, 128), (M - 128, N - 128, 128, 128), (M - 100, 0, 100, 128),
+             (0, N - 100, 128, 100), (40000, 20000, 128, 128)]
+    vs, bs = oracle_for(w, tiles=tiles)
+    for (i0, j0, mi, nj), v, b in zip(tiles, vs, bs):
+        got = D[i0:i0 + mi, j0:j0 + nj].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        check_bf16("bf16", got, v, b, what=f"huge {i0},{j0}")
+    del D
+    torch.cuda.empty_cache()
+
+
+def test_fp8_block_skinny_a_million_columns():
+    """N = 1,000,000 (7,813 N tiles, more than the SMs: the general stream-K
+    spread with the global workspace), ragged last tile."""
+    M, N, K = 16, 1_000_000, 256
+    w = fp8_case(M, N, K, seed=62, mode="block", out="bf16", outliers=0.01)
+    D = run(w)
+    torch.cuda.synchronize()
+    tiles = [(0, 0, M, 128), (0, N - 64, M, 64), (0, 500_032, M, 128)]
+    vs, bs = oracle_for(w, tiles=tiles)
+    for (i0, j0, mi, nj), v, b in zip(tiles, vs, bs):
+        got = D[:, j0:j0 + nj].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        check_bf16("fp8", got, v, b, what=f"1M columns {j0}")

@@ -212,3 +212,37 @@ def test_full_size(mode, rows, cols, in_dtype):
     else:
         x = synth.bf16(26, 2, rows, cols)
     check(x, mode)
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+def test_beyond_2_31_elements(mode):
+    """A 40,000 x 65,664 FP32 matrix (2.6e9 elements, 10.5 GB): a seeded
+    40-row slab repeated down the rows on the device; the last (partial) row
+    blocks and all of their scales are checked against the oracle."""
+    import tensor_core_dense_gb300 as tcg
+    R, C, SLAB = 40000, 65664, 40
+    slab = synth.values_f32(71, 1, SLAB, C, out_prob=0.01, out_factor=50.0)
+    X = torch.from_numpy(slab).cuda().repeat(R // SLAB, 1)
+    Q = torch.empty((R, C), dtype=torch.uint8, device="cuda")
+    n = tcg.quant_scale_count(R, C, MODES[mode])
+    S = torch.empty((n,), dtype=torch.float32, device="cuda")
+    tcg.quantize_e4m3(X, Q, S, mode=MODES[mode])
+    torch.cuda.synchronize()
+    del X
+    r0 = (R // 128) * 128                          # the last, 64-row block
+    host = slab[np.arange(r0, R) % SLAB]
+    KB = (C + 127) // 128
+    if mode == "tensor":
+        q_ref, s_ref = oracle.quantize_e4m3(slab, MODES[mode])
+        q_ref = q_ref[np.arange(r0, R) % SLAB]
+        s_got = S.cpu().numpy()
+    else:
+        q_ref, s_ref = oracle.quantize_e4m3(host, MODES[mode])
+        if mode == "block128":
+            s_got = S[(R // 128) * KB:].cpu().numpy()
+        else:  # scale[kb * R + r] for the last rows
+            s_got = S.view(KB, R)[:, r0:].contiguous().cpu().numpy().ravel()
+    assert np.array_equal(s_got.view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(Q[r0:].cpu().numpy(), q_ref)
+    del Q, S
+    torch.cuda.empty_cache()
