@@ -100,16 +100,18 @@ def _load():
         lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
         for name in ("orc_bf16_decode_array", "orc_bf16_encode_array",
                      "orc_e4m3_decode_array", "orc_e4m3_encode_array",
-                     "orc_e5m2_decode_array", "orc_cast_bf16_array"):
+                     "orc_e5m2_decode_array", "orc_e5m2_encode_array",
+                     "orc_cast_bf16_array"):
             getattr(lib, name).argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             getattr(lib, name).restype = None
         lib.orc_gemm_tiles.argtypes = [ctypes.POINTER(_Args), ctypes.c_int64, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.orc_gemm_tiles.restype = ctypes.c_int
         i64 = ctypes.c_int64
-        lib.orc_quant_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_int32, i64, i64, i64,
-                                       ctypes.c_int32, ctypes.c_void_p, i64, ctypes.c_void_p]
-        lib.orc_quant_e4m3.restype = ctypes.c_int
+        lib.orc_quant_fp8.argtypes = [ctypes.c_void_p, ctypes.c_int32, i64, i64, i64,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, i64,
+                                      ctypes.c_void_p]
+        lib.orc_quant_fp8.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -143,6 +145,11 @@ def e4m3_decode(bits) -> np.ndarray:
 def e5m2_decode(bits) -> np.ndarray:
     """E5M2 bytes -> float64 values (+-inf for S.11111.00, NaN for other S.11111.xx)."""
     return _elementwise("orc_e5m2_decode_array", bits, np.uint8, np.float64)
+
+
+def e5m2_encode(x) -> np.ndarray:
+    """float32 values -> E5M2 bytes, nearest even, saturating at +-57344."""
+    return _elementwise("orc_e5m2_encode_array", x, np.float32, np.uint8)
 
 
 def e4m3_encode(x) -> np.ndarray:
@@ -228,9 +235,14 @@ def gemm(M, N, K, A, lda, B, ldb, *, in_type=IN_BF16, scale_mode=SCALE_NONE,
 
 
 def quantize_e4m3(x, mode, *, ldq=None):
-    """FP8 E4M3 quantisation of a 2-D array x (float32 values, or uint16 BF16
-    bit patterns) with scale = amax / 448 per block (``oracle.c``,
-    orc_quant_e4m3).
+    """FP8 E4M3 quantisation (quantize_fp8 with fmt=FP8_E4M3)."""
+    return quantize_fp8(x, mode, FP8_E4M3, ldq=ldq)
+
+
+def quantize_fp8(x, mode, fmt, *, ldq=None):
+    """FP8 quantisation of a 2-D array x (float32 values, or uint16 BF16 bit
+    patterns) with scale = amax / 448 (FP8_E4M3) or amax / 57344 (FP8_E5M2)
+    per block (``oracle.c``, orc_quant_fp8).
 
     mode: Q_TENSOR (scale[0]), Q_ROW128 (scale[kb*rows + r]) or Q_BLOCK128
     (scale[rb*ceil(cols/128) + kb]).  Returns (q, scale): q is a rows x ldq
@@ -248,7 +260,8 @@ def quantize_e4m3(x, mode, *, ldq=None):
     n = {Q_TENSOR: 1, Q_ROW128: KB * rows, Q_BLOCK128: RB * KB}[mode]
     q = np.zeros((rows, ldq), dtype=np.uint8)
     s = np.zeros(max(n, 1), dtype=np.float32)
-    rc = _load().orc_quant_e4m3(_ptr(x), x_type, rows, cols, cols, mode, _ptr(q), ldq, _ptr(s))
+    rc = _load().orc_quant_fp8(_ptr(x), x_type, rows, cols, cols, mode, int(fmt), _ptr(q), ldq,
+                               _ptr(s))
     if rc != 0:
         raise ValueError("oracle rejected the quantiser arguments")
     return q, s[:n]

@@ -166,6 +166,48 @@ double orc_e5m2_decode(uint8_t b) {
   return s ? -mag : mag;
 }
 
+/* FP32 -> E5M2, round to nearest even on the E5M2 grid (2 fraction bits;
+ * subnormal step 2^-16 below 2^-14), saturating: a finite or infinite
+ * magnitude that rounds above 57344 becomes +-57344 (0x7B).  NaN -> 0x7F
+ * (sign kept).  Integer rounding on the FP32 significand, as for E4M3. */
+uint8_t orc_e5m2_encode(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+  uint32_t a = u & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return (uint8_t)(sign | 0x7Fu);
+  if (a == 0x7F800000u) return (uint8_t)(sign | 0x7Bu);
+  int ef = (int)(a >> 23);
+  if (ef == 0) return sign; /* below 2^-126: rounds to 0 */
+  uint64_t sig = (uint64_t)((a & 0x7FFFFFu) | 0x800000u); /* value = sig * 2^(E-23) */
+  int E = ef - 127;
+  int q = (E >= -14) ? E - 2 : -16; /* E5M2 quantum at this magnitude */
+  int shift = 23 + q - E;           /* >= 21 */
+  uint64_t r;
+  if (shift >= 40) {
+    r = 0;
+  } else {
+    uint64_t keep = sig >> shift;
+    uint64_t rem = sig & ((1ull << shift) - 1ull);
+    uint64_t half = 1ull << (shift - 1);
+    r = keep + ((rem > half || (rem == half && (keep & 1ull))) ? 1u : 0u);
+  }
+  if (q == -16 && r < 4) return (uint8_t)(sign | (uint8_t)r); /* subnormal r * 2^-16 */
+  int qq = q;
+  while (r >= 8) { /* carried into the next binade */
+    r >>= 1;
+    qq += 1;
+  }
+  /* value = r * 2^qq, 4 <= r <= 7, i.e. (1 + (r-4)/4) * 2^(qq+2) */
+  int efield = qq + 2 + 15;
+  if (efield > 30) return (uint8_t)(sign | 0x7Bu);
+  return (uint8_t)(sign | (uint8_t)(efield << 2) | (uint8_t)(r - 4));
+}
+
+void orc_e5m2_encode_array(const float* in, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e5m2_encode(in[i]);
+}
+
 void orc_e5m2_decode_array(const uint8_t* in, int64_t n, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e5m2_decode(in[i]);
 }
@@ -373,6 +415,9 @@ int orc_gemm_tiles(const orc_gemm_args* g, int64_t ntiles, const int64_t* tiles,
  * E4M3(x / s), i.e. the same as multiplying by 448 / amax up to the rounding
  * of that factor.
  *
+ * E5M2 (fmt 1) is the same with 57344, E5M2's maximum normal value, in place
+ * of 448 and the E5M2 encoder (orc_e5m2_encode).
+ *
  * Readings (the pages give the recipe, not these details):
  *  - amax is the largest |x| over the block, NaN entries ignored;
  *  - s = amax / 448 in FP32 (correctly rounded division); a block whose s is
@@ -400,47 +445,58 @@ static float quant_in(const void* X, int32_t x_type, int64_t idx) {
   return (float)orc_bf16_decode(((const uint16_t*)X)[idx]); /* exact: BF16 is FP32's top half */
 }
 
-/* Quantise the block rows r0..r1-1 x columns c0..c1-1; returns its scale. */
+/* Quantise the block rows r0..r1-1 x columns c0..c1-1 to E4M3 (fmt 0, top
+ * 448) or E5M2 (fmt 1, top 57344); returns its scale. */
 static float quant_block(const void* X, int32_t x_type, int64_t ldx, int64_t r0, int64_t r1,
-                         int64_t c0, int64_t c1, uint8_t* Q, int64_t ldq) {
+                         int64_t c0, int64_t c1, uint8_t* Q, int64_t ldq, int32_t fmt) {
   float amax = 0.0f;
   for (int64_t r = r0; r < r1; ++r)
     for (int64_t c = c0; c < c1; ++c) {
       float a = fabsf(quant_in(X, x_type, r * ldx + c));
       if (a > amax) amax = a; /* false for NaN: NaN entries are skipped */
     }
-  float s = amax / 448.0f;
+  float s = amax / (fmt == ORC_FP8_E5M2 ? 57344.0f : 448.0f);
   if (s == 0.0f) s = 1.0f;
   for (int64_t r = r0; r < r1; ++r)
     for (int64_t c = c0; c < c1; ++c) {
       float y = quant_in(X, x_type, r * ldx + c) / s;
-      Q[r * ldq + c] = (y != y) ? (uint8_t)0x7Fu : orc_e4m3_encode(y);
+      Q[r * ldq + c] = (y != y)                ? (uint8_t)0x7Fu
+                       : (fmt == ORC_FP8_E5M2) ? orc_e5m2_encode(y)
+                                               : orc_e4m3_encode(y);
     }
   return s;
 }
 
-int orc_quant_e4m3(const void* X, int32_t x_type, int64_t rows, int64_t cols, int64_t ldx,
-                   int32_t mode, uint8_t* Q, int64_t ldq, float* scale) {
+int orc_quant_fp8(const void* X, int32_t x_type, int64_t rows, int64_t cols, int64_t ldx,
+                  int32_t mode, int32_t fmt, uint8_t* Q, int64_t ldq, float* scale) {
   if (rows < 0 || cols < 0 || (x_type != 0 && x_type != 1) || !scale) return -1;
+  if (fmt != ORC_FP8_E4M3 && fmt != ORC_FP8_E5M2) return -1;
   if (rows > 0 && cols > 0 && (!X || !Q || ldx < cols || ldq < cols)) return -1;
   const int64_t KB = (cols + 127) / 128, RB = (rows + 127) / 128;
   if (mode == ORC_Q_TENSOR) {
-    scale[0] = quant_block(X, x_type, ldx, 0, rows, 0, cols, Q, ldq);
+    scale[0] = quant_block(X, x_type, ldx, 0, rows, 0, cols, Q, ldq, fmt);
   } else if (mode == ORC_Q_ROW128) {
     for (int64_t r = 0; r < rows; ++r)
       for (int64_t kb = 0; kb < KB; ++kb) {
         int64_t c1 = (kb + 1) * 128 < cols ? (kb + 1) * 128 : cols;
-        scale[kb * rows + r] = quant_block(X, x_type, ldx, r, r + 1, kb * 128, c1, Q, ldq);
+        scale[kb * rows + r] = quant_block(X, x_type, ldx, r, r + 1, kb * 128, c1, Q, ldq, fmt);
       }
   } else if (mode == ORC_Q_BLOCK128) {
     for (int64_t rb = 0; rb < RB; ++rb)
       for (int64_t kb = 0; kb < KB; ++kb) {
         int64_t r1 = (rb + 1) * 128 < rows ? (rb + 1) * 128 : rows;
         int64_t c1 = (kb + 1) * 128 < cols ? (kb + 1) * 128 : cols;
-        scale[rb * KB + kb] = quant_block(X, x_type, ldx, rb * 128, r1, kb * 128, c1, Q, ldq);
+        scale[rb * KB + kb] =
+            quant_block(X, x_type, ldx, rb * 128, r1, kb * 128, c1, Q, ldq, fmt);
       }
   } else {
     return -1;
   }
   return 0;
+}
+
+/* The E4M3 quantiser (fmt 0) under its original name. */
+int orc_quant_e4m3(const void* X, int32_t x_type, int64_t rows, int64_t cols, int64_t ldx,
+                   int32_t mode, uint8_t* Q, int64_t ldq, float* scale) {
+  return orc_quant_fp8(X, x_type, rows, cols, ldx, mode, ORC_FP8_E4M3, Q, ldq, scale);
 }

@@ -73,6 +73,24 @@ def test_e5m2_decode_matches_torch_float8_e5m2_for_all_codes():
     assert np.array_equal(ref[m], got[m]) and np.array_equal(np.signbit(ref[m]), np.signbit(got[m]))
 
 
+def test_e5m2_oracle_encoder_round_trip_torch_and_saturation():
+    codes = np.array([c for c in range(256) if np.isfinite(oracle.e5m2_decode(
+        np.array([c], np.uint8)))[0]], dtype=np.uint8)
+    assert np.array_equal(oracle.e5m2_encode(oracle.e5m2_decode(codes).astype(np.float32)), codes)
+    x = (np.random.default_rng(5).standard_normal(1 << 22) *
+         np.exp2(np.random.default_rng(6).integers(-24, 16, 1 << 22))).astype(np.float32)
+    x = x[np.abs(x) < 61440.0]
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e5m2_encode(x), ref)
+    big = np.array([57344.0, 61439.0, 61440.0, 1e9, np.inf], np.float32)
+    assert (oracle.e5m2_encode(big) == 0x7B).all() and (oracle.e5m2_encode(-big) == 0xFB).all()
+    # midpoints between neighbours round to the even code
+    pos = oracle.e5m2_decode(np.arange(0, 0x7B, dtype=np.uint8))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    got = oracle.e5m2_encode(mids).astype(int)
+    assert ((got % 2) == 0).all() and (np.abs(got - np.arange(0, 0x7A)) <= 1).all()
+
+
 def test_e5m2_generator_encoder_against_torch_and_decode():
     # the input generator's E5M2 encoder (test inputs only): round trip of every
     # finite code, nearest-even on 4M random values (torch's cast agrees inside
@@ -429,6 +447,10 @@ def test_bf16_error_bound_sanity_against_float32_gemm():
 # ("Tensor Cores", "Precision: FP16, BF16, TF32, FP8").
 
 Q_MODES = (oracle.Q_TENSOR, oracle.Q_ROW128, oracle.Q_BLOCK128)
+# per format: decoder, largest normal (the quantiser's target), its code,
+# torch's dtype, half a step relative to |x| for normals, half the subnormal step
+FMT = {oracle.FP8_E4M3: (oracle.e4m3_decode, 448.0, 0x7E, "float8_e4m3fn", 2.0 ** -4, 2.0 ** -10),
+       oracle.FP8_E5M2: (oracle.e5m2_decode, 57344.0, 0x7B, "float8_e5m2", 2.0 ** -3, 2.0 ** -17)}
 Q_SHAPES = [(1, 1), (3, 130), (128, 128), (130, 257), (257, 384), (64, 1000)]
 
 
@@ -449,82 +471,96 @@ def _nblocks(rows, cols, mode):
     return {oracle.Q_TENSOR: 1, oracle.Q_ROW128: rows * KB, oracle.Q_BLOCK128: RB * KB}[mode]
 
 
+@pytest.mark.parametrize("fmt", list(FMT))
 @pytest.mark.parametrize("mode", Q_MODES)
 @pytest.mark.parametrize("rows,cols", Q_SHAPES)
 @pytest.mark.parametrize("bf16_in", [False, True])
-def test_quant_power_of_two_blocks_reproduce_codes_and_scales(mode, rows, cols, bf16_in):
-    # X = decode(code) * 2^p_block with a +-448 in every block: the scale is
-    # exactly 2^p_block and every code comes back unchanged.  A wrong block
-    # geometry, scale index, missing |.| or misplaced division changes bits.
-    rng = np.random.default_rng(rows * 1000 + cols + 7 * mode)
+def test_quant_power_of_two_blocks_reproduce_codes_and_scales(mode, rows, cols, bf16_in, fmt):
+    # X = decode(code) * 2^p_block with the format's largest magnitude (448 or
+    # 57344) in every block: the scale is exactly 2^p_block and every code
+    # comes back unchanged.  A wrong block geometry, scale index, missing |.|
+    # or misplaced division changes bits.
+    dec, top, topcode, _, _, _ = FMT[fmt]
+    rng = np.random.default_rng(rows * 1000 + cols + 7 * mode + 97 * fmt)
     codes = rng.integers(0, 256, size=(rows, cols)).astype(np.uint8)
-    codes[(codes & 0x7F) == 0x7F] = 0x3A
+    if fmt == oracle.FP8_E4M3:
+        codes[(codes & 0x7F) == 0x7F] = 0x3A
+    else:
+        codes[(codes & 0x7C) == 0x7C] = 0x3A    # no E5M2 inf / NaN codes
     ids = _block_ids(rows, cols, mode)
     nb = _nblocks(rows, cols, mode)
     p = rng.integers(-20, 21, size=nb)
     flat_ids = ids.ravel()
     for b in range(nb):  # one +-448 per block, at a random member
         members = np.flatnonzero(flat_ids == b)
-        codes.flat[rng.choice(members)] = rng.choice([0x7E, 0xFE])
-    x = (oracle.e4m3_decode(codes) * np.exp2(p[ids])).astype(np.float32)
+        codes.flat[rng.choice(members)] = rng.choice([topcode, topcode | 0x80])
+    x = (dec(codes) * np.exp2(p[ids])).astype(np.float32)
     if bf16_in:  # E4M3 values times powers of two are exact in BF16
         xin = oracle.bf16_encode(x)
         assert np.array_equal(oracle.bf16_decode(xin).astype(np.float32), x)
     else:
         xin = x
-    q, s = oracle.quantize_e4m3(xin, mode)
+    q, s = oracle.quantize_fp8(xin, mode, fmt)
     assert np.array_equal(s, np.exp2(p).astype(np.float32))
     assert np.array_equal(q, codes)
 
 
+@pytest.mark.parametrize("fmt", list(FMT))
 @pytest.mark.parametrize("mode", Q_MODES)
-def test_quant_block_maximum_lands_on_448_and_zero_block_scale_one(mode):
+def test_quant_block_maximum_lands_on_448_and_zero_block_scale_one(mode, fmt):
+    dec, top, _, _, _, _ = FMT[fmt]
     rows, cols = 300, 520
     x = synth.values_f32(11, 1, rows, cols, out_prob=0.01, out_factor=50.0)
     x[:128, :128] = 0.0          # an all-zero 128 x 128 block (and 1 x 128 blocks)
     if mode == oracle.Q_TENSOR:
         x[:, :] = x * 3.0
-    q, s = oracle.quantize_e4m3(x, mode)
+    q, s = oracle.quantize_fp8(x, mode, fmt)
     ids = _block_ids(rows, cols, mode)
-    dq = np.abs(oracle.e4m3_decode(q))
+    dq = np.abs(dec(q))
     for b in range(_nblocks(rows, cols, mode)):
         m = ids == b
         amax = np.abs(x[m]).max()
         if amax == 0.0:
             assert s[b] == 1.0 and (q[m] == 0).all()
         else:
-            assert dq[m].max() == 448.0                      # the largest sits at 448
-            assert abs(float(s[b]) * 448.0 / float(amax) - 1.0) < 2.0 ** -23
+            assert dq[m].max() == top                        # the largest sits at the top
+            assert abs(float(s[b]) * top / float(amax) - 1.0) < 2.0 ** -23
 
 
+@pytest.mark.parametrize("fmt", list(FMT))
 @pytest.mark.parametrize("mode", Q_MODES)
-def test_quant_reconstruction_within_half_an_e4m3_step(mode):
-    # |decode(q) * s - x| <= half a quantum: 2^-4 |x| for normal codes, half the
-    # subnormal step 2^-9 (times s) below 2^-6; plus the FP32 division's rounding.
+def test_quant_reconstruction_within_half_an_e4m3_step(mode, fmt):
+    # |decode(q) * s - x| <= half a quantum: 2^-4 (E4M3) or 2^-3 (E5M2) of |x|
+    # for normal codes, half the subnormal step (times s) below the smallest
+    # normal; plus the FP32 division's rounding.
+    dec, _, _, _, rel, sub = FMT[fmt]
     rows, cols = 256, 384
     x = synth.values_f32(12, 1, rows, cols, out_prob=0.01, out_factor=50.0).astype(np.float32)
-    q, s = oracle.quantize_e4m3(x, mode)
+    q, s = oracle.quantize_fp8(x, mode, fmt)
     sel = s[_block_ids(rows, cols, mode)].astype(np.float64)
-    err = np.abs(oracle.e4m3_decode(q) * sel - x.astype(np.float64))
-    bound = 2.0 ** -4 * np.abs(x) * (1 + 2.0 ** -20) + 2.0 ** -10 * sel
+    err = np.abs(dec(q) * sel - x.astype(np.float64))
+    bound = rel * np.abs(x) * (1 + 2.0 ** -20) + sub * sel
     assert (err <= bound).all()
     # and it is not trivially loose: most elements sit well inside it
     assert np.median(err / bound) < 0.6
 
 
+@pytest.mark.parametrize("fmt", list(FMT))
 @pytest.mark.parametrize("mode", Q_MODES)
-def test_quant_matches_torch_division_and_float8_cast(mode):
+def test_quant_matches_torch_division_and_float8_cast(mode, fmt):
     # Given the scales, each code is torch's FP32 division followed by torch's
-    # float8_e4m3fn conversion; the scales are amax / 448 of numpy's max.
+    # float8_e4m3fn / float8_e5m2 conversion; the scales are amax / top of
+    # numpy's max.
+    _, top, _, tdt, _, _ = FMT[fmt]
     rows, cols = 200, 700
     x = synth.values_f32(13, 1, rows, cols, out_prob=0.01, out_factor=50.0)
-    q, s = oracle.quantize_e4m3(x, mode)
+    q, s = oracle.quantize_fp8(x, mode, fmt)
     ids = _block_ids(rows, cols, mode)
     amax = np.zeros(_nblocks(rows, cols, mode), dtype=np.float32)
     np.maximum.at(amax, ids.ravel(), np.abs(x).ravel())
-    assert np.array_equal(s, (torch.from_numpy(amax) / 448.0).numpy())
+    assert np.array_equal(s, (torch.from_numpy(amax) / top).numpy())
     y = torch.from_numpy(x) / torch.from_numpy(s[ids])
-    ref = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref = y.to(getattr(torch, tdt)).view(torch.uint8).numpy()
     assert np.array_equal(q, ref)
 
 
