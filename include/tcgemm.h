@@ -215,6 +215,19 @@ tcg_status quantize_e4m3(int64_t rows, int64_t cols, const void* X, int64_t ldx,
                          tcg_in_dtype x_dtype, tcg_quant_mode mode, void* Q, int64_t ldq,
                          float* scale, tcg_stream stream);
 
+/*
+ * quantize_fp8 -- quantize_e4m3 with the FP8 encoding chosen: TCG_FP8_E4M3
+ * (exactly quantize_e4m3) or TCG_FP8_E5M2, for which the scale is amax /
+ * 57344 (E5M2's largest normal value, "Tensor cores and low precision", FP8
+ * paragraph) and each code is the E5M2 value of the FP32 quotient, nearest
+ * even, saturating at +-57344; a NaN quotient gives 0x7F.  The pages suggest
+ * E5M2 for gradients.  Arguments, layouts, errors and work as quantize_e4m3;
+ * an unknown format returns TCG_ERR_UNSUPPORTED.
+ */
+tcg_status quantize_fp8(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                        tcg_in_dtype x_dtype, tcg_fp8_format format, tcg_quant_mode mode,
+                        void* Q, int64_t ldq, float* scale, tcg_stream stream);
+
 /* A static, human-readable name for a status code. */
 const char* tcg_status_string(tcg_status status);
 

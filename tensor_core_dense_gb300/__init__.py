@@ -29,7 +29,7 @@ QUANT_TENSOR, QUANT_ROW128, QUANT_BLOCK128 = 0, 1, 2
 
 # Every symbol include/tcgemm.h declares.
 EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8", "gemm_fp8_e4m3_block_noalloc",
-           "quantize_e4m3", "tcg_status_string", "tcg_last_device_status", "tcg_launch_count",
+           "quantize_e4m3", "quantize_fp8", "tcg_status_string", "tcg_last_device_status", "tcg_launch_count",
            "tcg_debug_timeout_probe")
 
 _lib = None
@@ -62,6 +62,8 @@ def lib():
         L.gemm_fp8.restype = i32
         L.quantize_e4m3.argtypes = [i64, i64, vp, i64, i32, i32, vp, i64, vp, vp]
         L.quantize_e4m3.restype = i32
+        L.quantize_fp8.argtypes = [i64, i64, vp, i64, i32, i32, i32, vp, i64, vp, vp]
+        L.quantize_fp8.restype = i32
         L.tcg_status_string.argtypes = [i32]
         L.tcg_status_string.restype = ctypes.c_char_p
         L.tcg_last_device_status.argtypes = [vp]
@@ -119,6 +121,10 @@ def gemm_fp8_raw(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale, b_scale, 
 
 def quantize_e4m3_raw(rows, cols, X, ldx, x_dtype, mode, Q, ldq, scale, stream) -> int:
     return int(lib().quantize_e4m3(rows, cols, X, ldx, x_dtype, mode, Q, ldq, scale, stream))
+
+
+def quantize_fp8_raw(rows, cols, X, ldx, x_dtype, fmt, mode, Q, ldq, scale, stream) -> int:
+    return int(lib().quantize_fp8(rows, cols, X, ldx, x_dtype, fmt, mode, Q, ldq, scale, stream))
 
 
 # --------------------------------------------------------------- tensor API
@@ -242,6 +248,12 @@ def quantize_e4m3(X, Q, scale, *, mode=QUANT_TENSOR, stream=None):
     """FP8 E4M3 codes into Q (uint8 or float8_e4m3fn, rows x >=cols) and
     dequantisation scales into `scale` (float32, quant_scale_count values) for
     the float32 or bfloat16 matrix X (layouts in include/tcgemm.h)."""
+    return quantize_fp8(X, Q, scale, mode=mode, fmt=FP8_E4M3, stream=stream)
+
+
+def quantize_fp8(X, Q, scale, *, mode=QUANT_TENSOR, fmt=FP8_E4M3, stream=None):
+    """quantize_e4m3 with the encoding chosen: FP8_E4M3 (scale amax/448) or
+    FP8_E5M2 (scale amax/57344); Q may be uint8 or the matching float8 dtype."""
     import torch
     if X.dtype == torch.float32:
         x_dtype = IN_F32
@@ -249,7 +261,7 @@ def quantize_e4m3(X, Q, scale, *, mode=QUANT_TENSOR, stream=None):
         x_dtype = IN_BF16
     else:
         raise ValueError("X must be float32 or bfloat16")
-    if Q.dtype not in (torch.uint8, torch.float8_e4m3fn):
+    if Q.dtype not in (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2):
         raise ValueError("Q must hold bytes")
     if scale.dtype != torch.float32 or not scale.is_contiguous():
         raise ValueError("scale must be a contiguous float32 tensor")
@@ -258,8 +270,8 @@ def quantize_e4m3(X, Q, scale, *, mode=QUANT_TENSOR, stream=None):
         raise ValueError("Q must be rows x (>= cols)")
     if scale.numel() < quant_scale_count(rows, cols, mode):
         raise ValueError("scale too small")
-    st = quantize_e4m3_raw(rows, cols, _ptr(X), _ld(X, "X"), x_dtype, mode, _ptr(Q), _ld(Q, "Q"),
-                           _ptr(scale), _stream_handle(stream))
+    st = quantize_fp8_raw(rows, cols, _ptr(X), _ld(X, "X"), x_dtype, fmt, mode, _ptr(Q),
+                          _ld(Q, "Q"), _ptr(scale), _stream_handle(stream))
     if st != OK:
-        raise TcgError(st, "quantize_e4m3")
+        raise TcgError(st, "quantize_fp8")
     return Q, scale

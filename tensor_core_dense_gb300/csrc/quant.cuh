@@ -1,14 +1,15 @@
-// quant.cuh -- FP8 E4M3 quantiser kernels (the C ABI entry point
-// quantize_e4m3 and its launch are in tcgemm.cu).
+// quant.cuh -- FP8 quantiser kernels, E4M3 and E5M2 (the C ABI entry points
+// quantize_fp8 / quantize_e4m3 and their launch are in tcgemm.cu).
 //
 // The FP8 recipe of "Tensor cores and low precision" (FP8 paragraph): a
 // tensor is rescaled so that its largest magnitudes land at E4M3's maximum
 // normal value, 448, then cast; the scale is removed after the product.
 // "Tensor Cores" ("Precision: FP16, BF16, TF32, FP8") names the granularities:
 // per tensor, per row, per block.  The stored (dequantisation) scale of a
-// block is s = amax / 448 and each code is E4M3(x / s) -- the FP32 quotient,
-// rounded to nearest even on the E4M3 grid, saturating at +-448 -- exactly the
-// codes and scales gemm_fp8_e4m3 consumes.
+// block is s = amax / top and each code is FP8(x / s) -- the FP32 quotient,
+// rounded to nearest even on the format's grid, saturating at +-top -- with
+// top = 448 for E4M3 and 57344 for E5M2 (the two encodings' largest normal
+// values, same page): exactly the codes and scales gemm_fp8 consumes.
 //
 // The work is a stream over X (read once, twice for one scale per tensor)
 // and Q (written once): HBM-bound, no tensor cores.  A persistent CTA per SM:
@@ -21,7 +22,7 @@
 //   ROW128    one box; each row is its own 1 x 128 block (warp-wide maximum)
 //   TENSOR    two launches over boxes: the maxima, folded into scale[0] with
 //             an integer atomicMax (bit patterns of non-negative floats order
-//             like the floats, and rounding a quotient by 448 is monotone, so
+//             like the floats, and rounding a quotient by the top is monotone, so
 //             the largest per-CTA s is s of the global maximum); then codes.
 //
 // Division.  Each code needs RN(x / s), the correctly rounded FP32 quotient.
@@ -94,10 +95,15 @@ __device__ __forceinline__ float warp_max(float m) {
   return m;
 }
 
+// Largest normal value of the FP8 format: E4M3 (kFmt 0) 448, E5M2 (1) 57344.
+template <int kFmt>
+__device__ __forceinline__ constexpr float quant_top() { return kFmt == 0 ? 448.0f : 57344.0f; }
+
 // Dequantisation scale for a block maximum; a zero quotient (all-zero block,
 // or underflow) becomes 1.
+template <int kFmt>
 __device__ __forceinline__ float quant_scale_of(float amax) {
-  const float s = __fdiv_rn(amax, 448.0f);
+  const float s = __fdiv_rn(amax, quant_top<kFmt>());
   return s == 0.0f ? 1.0f : s;
 }
 
@@ -126,10 +132,12 @@ __device__ __forceinline__ float quant_quotient(float x, const QuantDiv& d) {
   return __uint_as_float((__float_as_uint(q1) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
 }
 
-// Four codes E4M3(x / s), packed little-endian (first element in the low
+// Four codes FP8(x / s), packed little-endian (first element in the low
 // byte).  cvt.rn.satfinite rounds to nearest even, clamps finite overflow and
-// infinities to +-448 and turns a NaN of either sign into the canonical 0x7F
-// (checked on GB300 for +-NaN, +-inf, +-0, subnormal ties and 464).
+// infinities to the largest normal value and turns a NaN of either sign into
+// the canonical 0x7F (checked on GB300 for +-NaN, +-inf, +-0, subnormal ties
+// and the overflow midpoint, both formats).
+template <int kFmt>
 __device__ __forceinline__ uint32_t quant_encode4(const float (&v)[4], const QuantDiv& d) {
   float y[4];
   if (d.exact) {
@@ -140,8 +148,13 @@ __device__ __forceinline__ uint32_t quant_encode4(const float (&v)[4], const Qua
     for (int e = 0; e < 4; ++e) y[e] = quant_quotient(v[e], d);
   }
   uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(y[1]), "f"(y[0]));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(y[3]), "f"(y[2]));
+  if (kFmt == 0) {
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(y[1]), "f"(y[0]));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(y[3]), "f"(y[2]));
+  } else {
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(y[1]), "f"(y[0]));
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(y[3]), "f"(y[2]));
+  }
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
@@ -188,9 +201,9 @@ __device__ __forceinline__ bool quant_warp_wait(uint32_t bar, uint32_t parity,
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-template <int kIn, int kKind>
+template <int kIn, int kKind, int kFmt>
 __global__ void __launch_bounds__(kQThreads, 1)
-    quant_e4m3_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p) {
+    quant_fp8_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p) {
   constexpr uint32_t kStageBytes = kQBoxRows * kQBoxCols * (kIn == 0 ? 4u : 2u);
   constexpr int S = (int)(kQRingBytes / kStageBytes);
   extern __shared__ uint8_t smem_raw[];
@@ -313,14 +326,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
         m = slots[par * kQConsumerWarps];
 #pragma unroll
         for (int w = 1; w < kQConsumerWarps; ++w) m = fmaxf(m, slots[par * kQConsumerWarps + w]);
-        const QuantDiv d = quant_div(quant_scale_of(m));
+        const QuantDiv d = quant_div(quant_scale_of<kFmt>(m));
         if (threadIdx.x == 0) p.scale[u] = d.s;  // u = rb * KB + kb
 #pragma unroll
         for (int j = 0; j < kQBoxesPerBlock; ++j)
 #pragma unroll
           for (int i = 0; i < kQRowsPerWarp; ++i)
             quant_store4(p, r0 + j * kQBoxRows + warp * kQRowsPerWarp + i, c,
-                         quant_encode4(v[j * kQRowsPerWarp + i], d), full);
+                         quant_encode4<kFmt>(v[j * kQRowsPerWarp + i], d), full);
       } else {
         const int s = (int)(it % S);
         if (!quant_warp_wait(full_bar(s), (it / S) & 1u, abort_flag, 0x44)) {
@@ -342,14 +355,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
         } else if (kKind == kQuantEncode) {
 #pragma unroll
           for (int i = 0; i < kQRowsPerWarp; ++i)
-            quant_store4(p, rw + i, c, quant_encode4(v[i], tensor_div), full);
+            quant_store4(p, rw + i, c, quant_encode4<kFmt>(v[i], tensor_div), full);
         } else {  // ROW128: every row is a block
           float my_scale = 1.0f;
 #pragma unroll
           for (int i = 0; i < kQRowsPerWarp; ++i) {
-            const QuantDiv d = quant_div(quant_scale_of(warp_max(abs_max4(v[i]))));
+            const QuantDiv d = quant_div(quant_scale_of<kFmt>(warp_max(abs_max4(v[i]))));
             if (lane == i) my_scale = d.s;
-            quant_store4(p, rw + i, c, quant_encode4(v[i], d), full);
+            quant_store4(p, rw + i, c, quant_encode4<kFmt>(v[i], d), full);
           }
           if (lane < kQRowsPerWarp && rw + lane < p.rows)
             p.scale[(int64_t)(u % p.KB) * p.rows + rw + lane] = my_scale;
@@ -366,7 +379,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         float t = slots[0];
         for (int w = 1; w < kQConsumerWarps; ++w) t = fmaxf(t, slots[w]);
         // 0 for an all-zero tensor; the codes pass turns a final 0 into 1
-        atomicMax(reinterpret_cast<unsigned int*>(p.scale), __float_as_uint(__fdiv_rn(t, 448.0f)));
+        atomicMax(reinterpret_cast<unsigned int*>(p.scale),
+                  __float_as_uint(__fdiv_rn(t, quant_top<kFmt>())));
       }
     }
   }

@@ -552,10 +552,10 @@ tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, cuda
 
 // ------------------------------------------------------------ quantiser
 
-template <int kIn, int kKind>
+template <int kIn, int kKind, int kFmt>
 tcg_status launch_quant_inst(const CUtensorMap& map, const QuantParams& p, int grid, int dev,
                              cudaStream_t stream, bool pdl) {
-  auto* fn = &quant_e4m3_kernel<kIn, kKind>;
+  auto* fn = &quant_fp8_kernel<kIn, kKind, kFmt>;
   if (tcg_status s = ensure_smem(fn, kQSmemBytes, dev); s != TCG_OK) return s;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -572,7 +572,7 @@ tcg_status launch_quant_inst(const CUtensorMap& map, const QuantParams& p, int g
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
 
-template <int kIn>
+template <int kIn, int kFmt>
 tcg_status launch_quant(int64_t rows, int64_t cols, const void* X, int64_t ldx,
                         tcg_quant_mode mode, void* Q, int64_t ldq, float* scale,
                         cudaStream_t stream) {
@@ -601,20 +601,20 @@ tcg_status launch_quant(int64_t rows, int64_t cols, const void* X, int64_t ldx,
   p.units = (int32_t)units;
   const int grid = (int)(units < sms ? units : sms);
   if (mode == TCG_QUANT_BLOCK128)
-    return launch_quant_inst<kIn, kQuantBlock>(map, p, grid, dev, stream, false);
+    return launch_quant_inst<kIn, kQuantBlock, kFmt>(map, p, grid, dev, stream, false);
   if (mode == TCG_QUANT_ROW128)
-    return launch_quant_inst<kIn, kQuantRow>(map, p, grid, dev, stream, false);
+    return launch_quant_inst<kIn, kQuantRow, kFmt>(map, p, grid, dev, stream, false);
   // per tensor: clear the running maximum, fold the per-CTA maxima, encode.
   // X is kept in L2 between the two passes when it fits comfortably.
   int l2 = 0;
   if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) l2 = 0;
   p.keep_in_l2 = rows * ldx * esize <= (int64_t)l2 / 2 ? 1 : 0;
   if (cudaMemsetAsync(scale, 0, sizeof(float), stream) != cudaSuccess) return TCG_ERR_CUDA;
-  if (tcg_status s = launch_quant_inst<kIn, kQuantAmax>(map, p, grid, dev, stream, false);
+  if (tcg_status s = launch_quant_inst<kIn, kQuantAmax, kFmt>(map, p, grid, dev, stream, false);
       s != TCG_OK)
     return s;
   p.keep_in_l2 = 0;
-  return launch_quant_inst<kIn, kQuantEncode>(map, p, grid, dev, stream, true);
+  return launch_quant_inst<kIn, kQuantEncode, kFmt>(map, p, grid, dev, stream, true);
 }
 
 }  // namespace
@@ -702,10 +702,11 @@ tcg_status tcg_debug_timeout_probe(tcg_stream stream) {
   return TCG_OK;
 }
 
-tcg_status quantize_e4m3(int64_t rows, int64_t cols, const void* X, int64_t ldx,
-                         tcg_in_dtype x_dtype, tcg_quant_mode mode, void* Q, int64_t ldq,
-                         float* scale, tcg_stream stream) {
+tcg_status quantize_fp8(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                        tcg_in_dtype x_dtype, tcg_fp8_format format, tcg_quant_mode mode,
+                        void* Q, int64_t ldq, float* scale, tcg_stream stream) {
   if (x_dtype != TCG_IN_F32 && x_dtype != TCG_IN_BF16) return TCG_ERR_UNSUPPORTED;
+  if (format != TCG_FP8_E4M3 && format != TCG_FP8_E5M2) return TCG_ERR_UNSUPPORTED;
   if (mode != TCG_QUANT_TENSOR && mode != TCG_QUANT_ROW128 && mode != TCG_QUANT_BLOCK128)
     return TCG_ERR_UNSUPPORTED;
   if (rows < 0 || cols < 0) return TCG_ERR_INVALID_ARG;
@@ -725,8 +726,17 @@ tcg_status quantize_e4m3(int64_t rows, int64_t cols, const void* X, int64_t ldx,
       (uintptr_t)scale % 4 != 0)
     return TCG_ERR_ALIGNMENT;
   if (rows > INT32_MAX || cols > INT32_MAX) return TCG_ERR_UNSUPPORTED;
-  return x_dtype == TCG_IN_F32 ? launch_quant<0>(rows, cols, X, ldx, mode, Q, ldq, scale, st)
-                               : launch_quant<1>(rows, cols, X, ldx, mode, Q, ldq, scale, st);
+  if (format == TCG_FP8_E4M3)
+    return x_dtype == TCG_IN_F32 ? launch_quant<0, 0>(rows, cols, X, ldx, mode, Q, ldq, scale, st)
+                                 : launch_quant<1, 0>(rows, cols, X, ldx, mode, Q, ldq, scale, st);
+  return x_dtype == TCG_IN_F32 ? launch_quant<0, 1>(rows, cols, X, ldx, mode, Q, ldq, scale, st)
+                               : launch_quant<1, 1>(rows, cols, X, ldx, mode, Q, ldq, scale, st);
+}
+
+tcg_status quantize_e4m3(int64_t rows, int64_t cols, const void* X, int64_t ldx,
+                         tcg_in_dtype x_dtype, tcg_quant_mode mode, void* Q, int64_t ldq,
+                         float* scale, tcg_stream stream) {
+  return quantize_fp8(rows, cols, X, ldx, x_dtype, TCG_FP8_E4M3, mode, Q, ldq, scale, stream);
 }
 
 }  // extern "C"

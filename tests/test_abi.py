@@ -110,3 +110,9 @@ X, Q, S = 0x10000, 0x20000, 0x30000   # never dereferenced: validation fails fir
 ])
 def test_quant_host_validation(tcg, args, want):
     assert tcg.quantize_e4m3_raw(*args, None) == want
+
+
+
+def test_quant_fp8_format_validation(tcg):
+    # an unknown FP8 format is refused before anything runs
+    assert tcg.quantize_fp8_raw(8, 8, X, 8, 0, 7, 0, Q, 16, S, None) == 3

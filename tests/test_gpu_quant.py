@@ -38,7 +38,7 @@ def _pad(n, step):
     return -(-n // step) * step
 
 
-def gpu_quant(x, mode, *, ldx=None, ldq=None, reps=1):
+def gpu_quant(x, mode, *, ldx=None, ldq=None, reps=1, fmt=0):
     """Quantise x (float32 values or uint16 BF16 bits, rows x cols) on the GPU
     from a buffer with row pitch ldx into one with pitch ldq; returns (q, s,
     q_pad, s_extra): codes rows x cols, the scales, the untouched padding
@@ -58,17 +58,20 @@ def gpu_quant(x, mode, *, ldx=None, ldq=None, reps=1):
     n = tcg.quant_scale_count(rows, cols, mode)
     S = torch.full((n + 4,), float("nan"), dtype=torch.float32, device="cuda")
     for _ in range(reps):
-        tcg.quantize_e4m3(X[:, :cols], Q[:, :cols], S, mode=mode)
+        if fmt == 0:
+            tcg.quantize_e4m3(X[:, :cols], Q[:, :cols], S, mode=mode)
+        else:
+            tcg.quantize_fp8(X[:, :cols], Q[:, :cols], S, mode=mode, fmt=fmt)
     torch.cuda.synchronize()
     q = Q.cpu().numpy()
     s = S.cpu().numpy()
     return q[:, :cols], s[:n], q[:, cols:], s[n:]
 
 
-def check(x, mode_name, **kw):
+def check(x, mode_name, fmt=0, **kw):
     mode = MODES[mode_name]
-    q_ref, s_ref = oracle.quantize_e4m3(x, mode)
-    q, s, q_pad, s_extra = gpu_quant(x, mode, **kw)
+    q_ref, s_ref = oracle.quantize_fp8(x, mode, fmt)
+    q, s, q_pad, s_extra = gpu_quant(x, mode, fmt=fmt, **kw)
     assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32)), (
         f"scales differ at {np.flatnonzero(s.view(np.uint32) != s_ref.view(np.uint32))[:8]}")
     if not np.array_equal(q, q_ref):
@@ -127,18 +130,21 @@ def test_special_values(mode):
     check(x.astype(np.float32), mode)
 
 
-def _near_midpoint_blocks(seed, rows, cols):
+def _near_midpoint_blocks(seed, rows, cols, fmt=0):
     """Rows of 1 x 128 blocks, each with its own non-power-of-two maximum and
     127 values x whose quotients x / s lie within 3 FP32 units of a midpoint
-    between neighbouring E4M3 values (normal and subnormal)."""
+    between neighbouring E4M3 (or E5M2) values, normal and subnormal."""
     rng = np.random.default_rng(seed)
-    pos = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    if fmt == 0:
+        pos, top = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8)), 448.0
+    else:
+        pos, top = oracle.e5m2_decode(np.arange(0, 0x7C, dtype=np.uint8)), 57344.0
     mids = (pos[:-1] + pos[1:]) / 2
     x = np.zeros((rows, cols), np.float32)
     for r in range(rows):
         for kb in range(cols // 128):
-            amax = np.float32(448.0 * rng.uniform(0.5, 2.0) * 2.0 ** int(rng.integers(-40, 40)))
-            sc = np.float32(amax / np.float32(448.0))
+            amax = np.float32(top * rng.uniform(0.5, 2.0) * 2.0 ** int(rng.integers(-40, 40)))
+            sc = np.float32(amax / np.float32(top))
             vals = (rng.choice(mids, 127) * np.float64(sc)).astype(np.float32)
             vals = (vals.view(np.int32) + rng.integers(-3, 4, 127).astype(np.int32)).view(
                 np.float32) * rng.choice(np.array([-1.0, 1.0], np.float32), 127)
@@ -246,3 +252,29 @@ def test_beyond_2_31_elements(mode):
     assert np.array_equal(Q[r0:].cpu().numpy(), q_ref)
     del Q, S
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- E5M2 codes
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("rows,cols", [(1, 1), (5, 131), (130, 257), (16, 8192), (300, 1030)])
+def test_e5m2_shapes(mode, rows, cols):
+    check(synth.values_f32(81, 1, rows, cols, out_prob=0.01, out_factor=50.0), mode, fmt=1)
+    check(synth.bf16(82, 1, rows, cols, p1=2.0), mode, fmt=1)
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+def test_e5m2_division_near_midpoints_and_specials(mode):
+    check(_near_midpoint_blocks(83, 64, 1024, fmt=1), mode, fmt=1)
+    x = synth.values_f32(84, 1, 256, 384)
+    x[:128, :128] = 0.0
+    x[3, 200:204] = np.array([0x7FC00000, 0xFFC00000, 0x7F800001, 0xFF812345],
+                             np.uint32).view(np.float32)
+    x[130, 5] = -0.0
+    x[140, 140:200] = -1e-30
+    x[200, 300] = np.inf
+    check(x, mode, fmt=1)
+
+
+def test_e5m2_full_size_block_scaled_weight():
+    check(synth.values_f32(85, 2, 8192, 8192, out_prob=0.01, out_factor=50.0), "block128", fmt=1)
