@@ -65,8 +65,6 @@ struct QuantParams {
   int32_t rows, cols;
   int32_t KB;     // column blocks: ceil(cols / 128)
   int32_t units;  // BLOCK: ceil(rows/128) * KB; otherwise ceil(rows/kQBoxRows) * KB
-  int32_t keep_in_l2;  // TENSOR maxima pass: load X with an evict-last policy
-  int32_t pad_;
 };
 
 // Unit u -> first row, first column and number of boxes.
@@ -123,13 +121,36 @@ __device__ __forceinline__ QuantDiv quant_div(float s) {
   return d;
 }
 
-// RN(x / s) for a block whose s passed quant_div's range test.
-__device__ __forceinline__ float quant_quotient(float x, const QuantDiv& d) {
-  const float q0 = __fmaf_rn(x, d.r, __fmul_rn(x, d.r2));  // faithful
-  const float e = __fmaf_rn(-q0, d.s, x);                  // exact remainder
-  const float q1 = __fmaf_rn(e, d.r, q0);                  // correctly rounded
+// Two FP32 values as one 64-bit register pair, and back (the operand form of
+// Blackwell's packed f32x2 arithmetic).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// RN(x / s) for two elements of a block whose s passed quant_div's range
+// test: q0 = RN(x*r + RN(x*r')) (faithful), e = x - s*q0 (exact), q1 =
+// RN(q0 + e*r) (correctly rounded), each step one packed f32x2 operation
+// that rounds every lane exactly as the scalar instruction would.
+__device__ __forceinline__ void quant_quotient2(float x0, float x1, const QuantDiv& d, float& y0,
+                                                float& y1) {
+  const uint64_t x = pack_f32x2(x0, x1);
+  const uint64_t r = pack_f32x2(d.r, d.r), r2 = pack_f32x2(d.r2, d.r2);
+  const uint64_t ns = pack_f32x2(-d.s, -d.s);
+  uint64_t p, q0, e, q1;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(x), "l"(r2));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q0) : "l"(x), "l"(r), "l"(p));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns), "l"(x));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q1) : "l"(e), "l"(r), "l"(q0));
+  float a, b;
+  unpack_f32x2(q1, a, b);
   // the quotient has x's sign (s > 0); this also keeps -0 for x = -0
-  return __uint_as_float((__float_as_uint(q1) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+  y0 = __uint_as_float((__float_as_uint(a) & 0x7FFFFFFFu) | (__float_as_uint(x0) & 0x80000000u));
+  y1 = __uint_as_float((__float_as_uint(b) & 0x7FFFFFFFu) | (__float_as_uint(x1) & 0x80000000u));
 }
 
 // Four codes FP8(x / s), packed little-endian (first element in the low
@@ -144,8 +165,8 @@ __device__ __forceinline__ uint32_t quant_encode4(const float (&v)[4], const Qua
 #pragma unroll
     for (int e = 0; e < 4; ++e) y[e] = __fdiv_rn(v[e], d.s);
   } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) y[e] = quant_quotient(v[e], d);
+    quant_quotient2(v[0], v[1], d, y[0], y[1]);
+    quant_quotient2(v[2], v[3], d, y[2], y[3]);
   }
   uint16_t lo, hi;
   if (kFmt == 0) {
@@ -237,7 +258,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap);
-      const uint64_t policy = p.keep_in_l2 ? l2_policy_evict_last() : l2_policy_evict_first();
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
@@ -251,8 +271,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-          tma_load_2d_hint(smem_u32(smem + (uint32_t)s * kStageBytes), &tmap, full_bar(s), c0,
-                           r0 + j * kQBoxRows, policy);
+          tma_load_2d(smem_u32(smem + (uint32_t)s * kStageBytes), &tmap, full_bar(s), c0,
+                      r0 + j * kQBoxRows);
         }
       }
       if (!ok) {

@@ -605,15 +605,12 @@ tcg_status launch_quant(int64_t rows, int64_t cols, const void* X, int64_t ldx,
   if (mode == TCG_QUANT_ROW128)
     return launch_quant_inst<kIn, kQuantRow, kFmt>(map, p, grid, dev, stream, false);
   // per tensor: clear the running maximum, fold the per-CTA maxima, encode.
-  // X is kept in L2 between the two passes when it fits comfortably.
-  int l2 = 0;
-  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) l2 = 0;
-  p.keep_in_l2 = rows * ldx * esize <= (int64_t)l2 / 2 ? 1 : 0;
+  // (Loading X with an evict-last policy in the first pass did not keep it in
+  // L2 for the second on GB300; both passes read it from HBM.)
   if (cudaMemsetAsync(scale, 0, sizeof(float), stream) != cudaSuccess) return TCG_ERR_CUDA;
   if (tcg_status s = launch_quant_inst<kIn, kQuantAmax, kFmt>(map, p, grid, dev, stream, false);
       s != TCG_OK)
     return s;
-  p.keep_in_l2 = 0;
   return launch_quant_inst<kIn, kQuantEncode, kFmt>(map, p, grid, dev, stream, true);
 }
 
