@@ -296,7 +296,8 @@ def time_graph(rot, steps, warmup):
     return e0.elapsed_time(e1), launches, g
 
 
-SECONDARY = ("fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64", "fp8_skinny_128")
+SECONDARY = ("bf16_256", "fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64",
+             "fp8_skinny_128")
 
 # The FP8 quantiser on the operands the FP8 workloads cast: (seed, tensor id,
 # rows, cols, granularity, outlier probability).  The values are the FP32

@@ -99,8 +99,9 @@ tcg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
  *                    scales sa[i,kb] * sb[j/128,kb] ("promotion": partial sums
  *                    moved to FP32 at intervals, "Tensor Cores: Matrix
  *                    Instructions, Swizzling and FP8, Measured", Step 5).
- *                    Supported for M <= 128 (the skinny/decode shape); larger
- *                    M returns TCG_ERR_UNSUPPORTED.
+ *                    Any M: the kernel is built for M <= 128 (the skinny,
+ *                    decode-sized shape, one chunk of A); larger M runs in
+ *                    chunks of 128 rows of A, each output tile 128 x 128.
  */
 tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                          const void* B, int64_t ldb, const float* a_scale, const float* b_scale,
@@ -141,10 +142,10 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  * inside the library's device code, present on every device that loads the
  * library until the process exits; the caller still provides A, B, the
  * scales, C and D.  A problem whose scratch would exceed 32 MiB (counters:
- * ceil(N/128) words rounded up to 256 bytes; partial sums: ceil(N/128) x
- * segments-per-tile x Mp x 128 FP32 values, Mp = M rounded up to 16/32/64/128)
- * is rejected with TCG_ERR_UNSUPPORTED before anything is enqueued; M > 128
- * is rejected the same way.
+ * ceil(N/128) words rounded up to 256 bytes; partial sums: two Mp x 128 FP32
+ * tiles per CTA of the launch, at most 152 CTAs x 64 KB; Mp = M rounded up to
+ * 16/32/64/128) is rejected with TCG_ERR_UNSUPPORTED before anything is
+ * enqueued; M > 128 is rejected the same way.
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and raises the kernel's shared-memory limit; make that

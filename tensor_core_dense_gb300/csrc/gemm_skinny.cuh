@@ -1,4 +1,5 @@
-// gemm_skinny.cuh -- FP8 E4M3 GEMM with 128-block scales for skinny M (<= 128).
+// gemm_skinny.cuh -- FP8 GEMM with 128-block scales, swap-AB: skinny M (<= 128)
+// in one chunk, larger M in chunks of 128 rows.
 //
 //   D[m, n] = alpha * sum_kb sa[kb*M + m] * sb[(n/128)*KB + kb]
 //                    * sum_{k in block kb} qa[m, k] * qb[n, k]   (+ beta * C)
@@ -10,6 +11,9 @@
 // values of K forces each K block to be summed on its own and promoted into
 // an FP32 accumulator, the periodic promotion of "Tensor Cores: Matrix
 // Instructions, Swizzling and FP8, Measured", Step 5.
+//
+// Larger M is cut into chunks of 128 rows of A: a tile is then (N tile, M
+// chunk), a 128 x 128 block of D, with the same steps and promotion.
 //
 // Skinny M (a decode-sized batch) cannot fill UMMA's M >= 64 rows ("How
 // Blackwell's Tensor Memory Actually Works", "What this does to serving
@@ -84,6 +88,8 @@ struct SkinnyCfg {
 struct SkinnyParams {
   int32_t M, N, K;
   int32_t n_tiles, num_kb, total_steps, grid, max_seg;
+  int32_t m_tiles;   // M in chunks of kMp rows (1 when M <= 128)
+  int32_t pad_m_;
   const float* a_scale;  // [KB][M]
   const float* b_scale;  // [ceil(N/128)][KB]
   const void* C;
@@ -94,9 +100,17 @@ struct SkinnyParams {
   int32_t out_f32, has_c;
   uint32_t fp8_fmt;  // UMMA A (= B, the weights) / UMMA B (= A) format fields
   int32_t pad_;
-  float* ws;               // [n_tiles][max_seg][Mp][128] partial sums
-  unsigned int* counters;  // [n_tiles], zero between calls
+  float* ws;               // [grid][2][Mp][128] partial sums: a CTA's first and last piece
+  unsigned int* counters;  // [n_tiles * m_tiles], zero between calls
 };
+
+// Tile t (of n_tiles * m_tiles) -> N tile and M chunk.  Tiles that share an
+// N tile (the same slab of B, the HBM stream) are consecutive, so CTAs working
+// on different M chunks of one slab read it at about the same time.
+__host__ __device__ __forceinline__ void sk_tile(int t, int m_tiles, int& ntile, int& mt) {
+  ntile = t / m_tiles;
+  mt = t - ntile * m_tiles;
+}
 
 __host__ __device__ __forceinline__ int64_t sk_range_start(int64_t c, int64_t T, int64_t G) {
   return c * T / G;
@@ -161,7 +175,9 @@ __device__ __forceinline__ void emit_four(const SkinnyParams& p, int m, int n, f
   }
 }
 
-template <int kMp, bool kPair>
+// kMChunks: M > 128, A in chunks of kMp = 128 rows.  Without it m_tiles is the
+// constant 1, so the chunk index folds away (M <= 128 keeps its lean code).
+template <int kMp, bool kPair, bool kMChunks>
 __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     gemm_fp8_block_skinny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                  const __grid_constant__ CUtensorMap tmap_b,
@@ -203,6 +219,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
   const int64_t s0 = sk_range_start(blockIdx.x, T, G);
   const int64_t s1 = sk_range_start(blockIdx.x + 1, T, G);
   const int KB = p.num_kb;
+  const int32_t m_tiles = kMChunks ? p.m_tiles : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -247,7 +264,10 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
       uint32_t j = 0;
       bool ok = true;
       for (int64_t st = s0; st < s1; ++st, ++j) {
-        const int nt = (int)(st / KB), kb = (int)(st % KB);
+        const int q = (int)st / KB;  // steps fit in 32 bits (checked at launch)
+        const int kb = (int)st - q * KB;
+        int nt, mt;
+        sk_tile(q, m_tiles, nt, mt);
         const uint32_t s = j % S, ph = (j / S) & 1u;
         if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, 0x11)) {
           ok = false;
@@ -255,7 +275,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
         }
         mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
         tma_load_2d_hint(b_smem(s), &tmap_b, full_bar(s), kb * 128, nt * 128, stream_policy);
-        tma_load_2d_hint(a_smem(s), &tmap_a, full_bar(s), kb * 128, 0, keep_policy);
+        tma_load_2d_hint(a_smem(s), &tmap_a, full_bar(s), kb * 128, mt * kMp, keep_policy);
       }
       grid_launch_dependents();  // every load is issued: the next kernel may launch
       if (!ok) {
@@ -346,12 +366,15 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
             va[e] = 0.0f;
             vb[e] = 0.0f;
             if (idx < n) {
-              const int64_t gst = tab_begin + idx / kMp;
-              const int m = idx % kMp;
-              const int64_t tnt = gst / KB, tkb = gst % KB;
+              const int gst = (int)tab_begin + idx / kMp;
+              const int q = gst / KB;
+              const int tkb = gst - q * KB;
+              int tnt, tmt;
+              sk_tile(q, m_tiles, tnt, tmt);
+              const int m = tmt * kMp + idx % kMp;
               if (m < p.M) {
-                va[e] = __ldg(p.a_scale + tkb * p.M + m);
-                vb[e] = __ldg(p.b_scale + tnt * KB + tkb);
+                va[e] = __ldg(p.a_scale + (int64_t)tkb * p.M + m);
+                vb[e] = __ldg(p.b_scale + (int64_t)tnt * KB + tkb);
               }
             }
           }
@@ -366,8 +389,8 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
           break;
         }
       }
-      const int nt = (int)(st / KB);
-      const int kb = (int)(st - (int64_t)nt * KB);
+      const int nt = (int)st / KB;  // tile index (N tile and M chunk)
+      const int kb = (int)st - nt * KB;
       const uint32_t b = j % kSkNumAcc, bph = (j / kSkNumAcc) & 1u;
       uint32_t got = 0;
       if (lane == 0) got = wait_phase(tfull_bar(b), bph, abort_flag, 0x14) ? 1u : 0u;
@@ -409,15 +432,17 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) part[(col0 + c) * 128 + nloc] = acc[c];
       } else if (kb_first == 0 && kb == KB - 1) {
-        const int n = nt * 128 + nloc;
+        int ntile, mt;
+        sk_tile(nt, m_tiles, ntile, mt);
+        const int n = ntile * 128 + nloc;
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) emit_one(p, col0 + c, n, acc[c]);
+        for (int c = 0; c < kHalf; ++c) emit_one(p, mt * kMp + col0 + c, n, acc[c]);
       } else {
-        // partial tile: park it in this CTA's workspace slot; the handshake
-        // waits for the end of the range
-        const int64_t first_owner = sk_owner(tile_first, T, G);
-        const int slot = (int)((int64_t)blockIdx.x - first_owner);
-        float* wsp = p.ws + ((int64_t)nt * p.max_seg + slot) * kMp * 128;
+        // partial tile: park it in this CTA's workspace slot (0 for the
+        // first tile of its range, 1 for the last); the handshake waits for
+        // the end of the range
+        const int slot = nt == (int)s0 / KB ? 0 : 1;
+        float* wsp = p.ws + ((int64_t)blockIdx.x * 2 + slot) * kMp * 128;
 #pragma unroll
         for (int c = 0; c < kHalf; ++c) __stcg(wsp + (int64_t)(col0 + c) * 128 + nloc, acc[c]);
         pend_nt[npend++] = nt;
@@ -454,8 +479,17 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
           if (!last_flag[i]) continue;
           const int tnt = pend_nt[i];
           const int64_t tf = (int64_t)tnt * KB;
-          const int nseg = (int)(sk_owner(tf + KB - 1, T, G) - sk_owner(tf, T, G) + 1);
-          const float* wt = p.ws + (int64_t)tnt * p.max_seg * kMp * 128;
+          const int64_t first_owner = sk_owner(tf, T, G);
+          const int nseg = (int)(sk_owner(tf + KB - 1, T, G) - first_owner + 1);
+          // contributor sgi is CTA first_owner + sgi; its slot for this tile
+          // is 0 if the tile is the first of its range, else 1
+          const float4* src[kSkMaxSeg];
+#pragma unroll
+          for (int sgi = 0; sgi < kSkMaxSeg; ++sgi) {
+            const int64_t c = first_owner + (sgi < nseg ? sgi : 0);
+            const int slot = tnt == (int)sk_range_start(c, T, G) / KB ? 0 : 1;
+            src[sgi] = reinterpret_cast<const float4*>(p.ws + (c * 2 + slot) * kMp * 128);
+          }
           // All epilogue threads sum the slots (in slot order) over float4
           // units of the Mp x 128 tile: a warp covers 32 consecutive units (one
           // row m), kU units x all slots in flight per thread.
@@ -468,10 +502,8 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
             for (int sgi = 0; sgi < kSkMaxSeg; ++sgi)
 #pragma unroll
               for (int v = 0; v < kU; ++v)
-                part[sgi][v] = sgi < nseg
-                                   ? __ldcg(reinterpret_cast<const float4*>(wt) +
-                                            (int64_t)sgi * kUnits + u0 + v * kSkEpiThreads + etid)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                part[sgi][v] = sgi < nseg ? __ldcg(src[sgi] + u0 + v * kSkEpiThreads + etid)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int v = 0; v < kU; ++v) {
               float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -485,7 +517,9 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
                 }
               }
               const int u = u0 + v * kSkEpiThreads + etid;
-              emit_four(p, u >> 5, tnt * 128 + (u & 31) * 4, sum);
+              int ntile, mt;
+              sk_tile(tnt, m_tiles, ntile, mt);
+              emit_four(p, mt * kMp + (u >> 5), ntile * 128 + (u & 31) * 4, sum);
             }
           }
         }
@@ -505,13 +539,14 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
       const uint32_t local = smem_u32(gbase);
       const uint32_t lo_half = map_shared_to_cta(local, 0);  // K blocks [0, KB/2)
       const uint32_t hi_half = map_shared_to_cta(local, 1);
-      const int tnt = (int)(s0 / KB);
+      int tnt, tmt;
+      sk_tile((int)s0 / KB, m_tiles, tnt, tmt);
       const int etid = (int)((warp - 2) * 32u + lane);
       for (int u = (int)rank * (kUnits / 2) + etid; u < ((int)rank + 1) * (kUnits / 2);
            u += kSkEpiThreads) {
         const float4 a = ld_shared_cluster_v4(lo_half + 16u * (uint32_t)u);
         const float4 b = ld_shared_cluster_v4(hi_half + 16u * (uint32_t)u);
-        emit_four(p, u >> 5, tnt * 128 + (u & 31) * 4,
+        emit_four(p, tmt * kMp + (u >> 5), tnt * 128 + (u & 31) * 4,
                   make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
       }
     }

@@ -187,38 +187,43 @@ tcg_status tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, const void* p
 
 struct Workspace {
   void* ptr = nullptr;
-  size_t bytes = 0;
+  size_t counter_cap = 0;  // bytes reserved for tile counters at the start
+  size_t partial_cap = 0;  // bytes of partial slots after them
 };
 Workspace g_ws[kMaxDevices];
 std::mutex g_ws_mu;
 
-// Per-device workspace: counters (n_tiles words, kept zero between calls)
-// followed by the FP32 partial slots.  Grown on demand, never shrunk.
+// Per-device workspace: tile counters (one word per tile, kept zero between
+// calls) in a region of their own at the start, then the FP32 partial slots.
+// Both regions only grow; the partials always start after the whole counter
+// region, so no call's partial sums land on counter words a later call with
+// more tiles relies on being zero.
 tcg_status get_workspace(int dev, size_t counter_bytes, size_t partial_bytes, cudaStream_t stream,
                          unsigned int** counters, float** partials) {
   const size_t cbytes = (counter_bytes + 255) & ~size_t(255);
-  const size_t need = cbytes + partial_bytes;
   std::lock_guard<std::mutex> lk(g_ws_mu);
   Workspace& w = g_ws[dev];
-  if (w.bytes < need) {
+  if (w.counter_cap < cbytes || w.partial_cap < partial_bytes) {
+    const size_t ccap = w.counter_cap > cbytes ? w.counter_cap : cbytes;
+    const size_t pcap = w.partial_cap > partial_bytes ? w.partial_cap : partial_bytes;
     if (w.ptr) {
       if (cudaDeviceSynchronize() != cudaSuccess) return TCG_ERR_CUDA;
       cudaFree(w.ptr);
       w.ptr = nullptr;
-      w.bytes = 0;
+      w.counter_cap = w.partial_cap = 0;
     }
     void* p = nullptr;
-    if (cudaMalloc(&p, need) != cudaSuccess) return TCG_ERR_CUDA;
-    // counters must start at zero; the region past the old size is new
-    if (cudaMemsetAsync(p, 0, need, stream) != cudaSuccess) {
+    if (cudaMalloc(&p, ccap + pcap) != cudaSuccess) return TCG_ERR_CUDA;
+    if (cudaMemsetAsync(p, 0, ccap, stream) != cudaSuccess) {  // counters start at zero
       cudaFree(p);
       return TCG_ERR_CUDA;
     }
     w.ptr = p;
-    w.bytes = need;
+    w.counter_cap = ccap;
+    w.partial_cap = pcap;
   }
   *counters = static_cast<unsigned int*>(w.ptr);
-  *partials = reinterpret_cast<float*>(static_cast<char*>(w.ptr) + cbytes);
+  *partials = reinterpret_cast<float*>(static_cast<char*>(w.ptr) + w.counter_cap);
   return TCG_OK;
 }
 
@@ -474,8 +479,10 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   p.N = (int32_t)a.N;
   p.K = (int32_t)a.K;
   p.n_tiles = (int32_t)((a.N + 127) / 128);
+  p.m_tiles = (int32_t)((a.M + kMp - 1) / kMp);  // 1 unless M > 128 (kMp = 128)
   p.num_kb = (int32_t)((a.K + 127) / 128);
-  const int64_t T = (int64_t)p.n_tiles * p.num_kb;
+  const int64_t tiles = (int64_t)p.n_tiles * p.m_tiles;
+  const int64_t T = tiles * p.num_kb;
   if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
   p.total_steps = (int32_t)T;
   // With fewer N tiles than SMs, each tile's K range is cut into
@@ -486,11 +493,11 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   int64_t split = 0;
   {
     int64_t g;
-    if (p.n_tiles < sms) {
-      split = sms / p.n_tiles;
+    if (tiles < sms) {
+      split = sms / tiles;
       if (split > 3) split = 3;
       if (split > p.num_kb) split = p.num_kb;
-      g = p.n_tiles * split;
+      g = tiles * split;
     } else {
       const int64_t min_steps = (p.num_kb + 2) / 3;
       g = T / min_steps;
@@ -512,7 +519,8 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   if (split == 2) {
     // two halves per tile: a cluster of the two CTAs joins them in shared
     // memory (no workspace)
-    auto* fn = &gemm_fp8_block_skinny_kernel<kMp, true>;
+    auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, true, kMp == 128>
+                             : &gemm_fp8_block_skinny_kernel<kMp, true, false>;
     if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
     if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 2, ma, mb, p) !=
         cudaSuccess)
@@ -526,13 +534,15 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);
   if (p.max_seg > p.grid) p.max_seg = p.grid;
   if (p.num_kb > 1) {  // a tile may be split over CTAs: needs the workspace
-    const size_t partial_bytes = (size_t)p.n_tiles * p.max_seg * kMp * 128 * sizeof(float);
-    if (tcg_status s = get_workspace(dev, (size_t)p.n_tiles * sizeof(unsigned int),
+    // two partial-tile slots per CTA (the first and the last piece of its range)
+    const size_t partial_bytes = (size_t)p.grid * 2 * kMp * 128 * sizeof(float);
+    if (tcg_status s = get_workspace(dev, (size_t)tiles * sizeof(unsigned int),
                                      partial_bytes, stream, &p.counters, &p.ws);
         s != TCG_OK)
       return s;
   }
-  auto* fn = &gemm_fp8_block_skinny_kernel<kMp, false>;
+  auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, false, kMp == 128>
+                           : &gemm_fp8_block_skinny_kernel<kMp, false, false>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
   if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 1, ma, mb, p) !=
       cudaSuccess)
@@ -650,8 +660,7 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   if (K == 0) return launch_k0(a, st);
   if (!a_scale || !b_scale) return TCG_ERR_INVALID_ARG;
   if (mode == TCG_SCALE_TENSOR) return launch_tn<1>(a, a_scale, b_scale, st);
-  if (M > 128) return TCG_ERR_UNSUPPORTED;
-  return launch_skinny(a, a_scale, b_scale, st);
+  return launch_skinny(a, a_scale, b_scale, st);  // any M: M > 128 in 128-row chunks
 }
 
 tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
@@ -685,7 +694,7 @@ tcg_status tcg_last_device_status(tcg_stream stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
     std::lock_guard<std::mutex> lk(g_ws_mu);
-    if (g_ws[dev].ptr) cudaMemset(g_ws[dev].ptr, 0, g_ws[dev].bytes);
+    if (g_ws[dev].ptr) cudaMemset(g_ws[dev].ptr, 0, g_ws[dev].counter_cap);
   }
   return TCG_ERR_TIMEOUT;
 }
@@ -805,6 +814,7 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
   p.N = (int32_t)a.N;
   p.K = (int32_t)a.K;
   p.n_tiles = (int32_t)((a.N + 127) / 128);
+  p.m_tiles = 1;  // M <= 128 on this path
   p.num_kb = (int32_t)((a.K + 127) / 128);
   const int64_t T = (int64_t)p.n_tiles * p.num_kb;
   if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
@@ -832,7 +842,7 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
   p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);
   if (p.max_seg > p.grid) p.max_seg = p.grid;
   const size_t counter_bytes = ((size_t)p.n_tiles * sizeof(unsigned int) + 255) & ~size_t(255);
-  const size_t partial_bytes = (size_t)p.n_tiles * p.max_seg * kMp * 128 * sizeof(float);
+  const size_t partial_bytes = (size_t)p.grid * 2 * kMp * 128 * sizeof(float);
   if (counter_bytes + partial_bytes > kNoAllocScratchBytes) return TCG_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   if (tcg_status s = noalloc_scratch(dev, &scratch); s != TCG_OK) return s;
@@ -854,7 +864,7 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
   p.beta = a.beta;
   p.out_f32 = a.out == TCG_OUT_F32;
   p.has_c = a.beta != 0.0f;
-  auto* fn = &gemm_fp8_block_skinny_kernel<kMp, false>;
+  auto* fn = &gemm_fp8_block_skinny_kernel<kMp, false, false>;  // M <= 128: one chunk
   {  // raise the shared-memory limit once per device (no host-side table)
     static bool raised[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(g_noalloc_mu);

@@ -230,7 +230,7 @@ def test_fp8_block_skinny_shapes(M, N, K, out, beta):
 
 
 @pytest.mark.parametrize("M,N,K", [(5, 260, 300), (64, 1024, 4096), (128, 2048, 2048),
-                                   (20, 8192, 640)])
+                                   (20, 8192, 640), (300, 260, 384), (256, 4096, 512)])
 def test_fp8_block_scale_indexing_bit_exact(M, N, K):
     """Power-of-two block scales that depend on (row, K block) and (N block,
     K block) with small-integer codes: every misplaced scale changes bits."""
@@ -252,7 +252,32 @@ def test_fp8_block_scale_indexing_bit_exact(M, N, K):
     assert np.array_equal(d_to_host(run(w)).astype(np.float64), v)
 
 
-@pytest.mark.parametrize("M,N", [(64, 4096), (16, 8192)])
+# M > 128: A in chunks of 128 rows, each tile a 128 x 128 block of D (the
+# general split, the cluster pair at 64 tiles, unsplit tiles at 128 tiles).
+@pytest.mark.parametrize("M,N,K", [(129, 256, 512), (300, 1000, 1024), (256, 4096, 512),
+                                   (1024, 2048, 1536), (777, 3000, 2200)])
+@pytest.mark.parametrize("out,beta", [("f32", 0.0), ("bf16", 1.0)])
+def test_fp8_block_scaled_large_m(M, N, K, out, beta):
+    w = fp8_case(M, N, K, seed=M + 3 * N + K, mode="block", out=out, beta=beta, outliers=0.01)
+    check_full(w, run(w))
+
+
+def test_fp8_block_workspace_reuse_across_shapes():
+    """A call with many tiles, one with few (whose partial sums must not land
+    on counter words), then the first shape again: all three correct."""
+    many = fp8_case(600, 4096, 1024, seed=91, mode="block", out="f32", outliers=0.01)
+    few = fp8_case(16, 1000, 2048, seed=92, mode="block", out="f32", outliers=0.01)
+    for w in (many, few, many, few):
+        check_full(w, run(w))
+
+
+def test_fp8_block_scaled_4096_cubed_sampled():
+    w = fp8_case(4096, 4096, 4096, seed=17, mode="block", out="bf16", outliers=0.01)
+    _sampled(w, out="f32")
+    _sampled(w, out="bf16")
+
+
+@pytest.mark.parametrize("M,N", [(64, 4096), (16, 8192), (600, 2048)])
 def test_fp8_block_skinny_deterministic(M, N):
     w = fp8_case(M, N, 4096, seed=11, mode="block", out="f32", outliers=0.01)
     d1 = d_to_host(run(w))

@@ -92,11 +92,18 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
         pytest.skip("no CUDA device")
     import tensor_core_dense_gb300 as tcg
     fn = _noalloc_fn()
-    M, N, K = 128, 65536, 8192   # needs 64 MiB of partial sums: over the 32 MiB array
+    # The buffers below are far smaller than the problem, so this call must be
+    # refused by the host before anything is launched.  Its tile counters
+    # alone (one 4-byte word per 128 columns of N: 64 MiB here) exceed the
+    # 32 MiB array, whatever the partial-sum layout.  Check that arithmetic
+    # here first, so a change to the scratch sizing fails this test instead
+    # of launching a kernel over undersized buffers.
+    M, N, K = 128, (1 << 31) - 128, 8192
+    counter_bytes = -(-N // 128) * 4
+    assert counter_bytes > 32 << 20, "this rejection case no longer exceeds the scratch array"
     A = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
     sa = torch.ones(M * (K // 128), device="cuda")
     D = torch.empty((M, 16), dtype=torch.float32, device="cuda")
-    # B is never read: the size check fails first
     st = fn(M, N, K, A.data_ptr(), K, A.data_ptr(), K, sa.data_ptr(), sa.data_ptr(), None, 0,
             D.data_ptr(), N, tcg.OUT_F32, 1.0, 0.0, torch.cuda.current_stream().cuda_stream)
     assert st == tcg.ERR_UNSUPPORTED
