@@ -121,17 +121,6 @@ __device__ __forceinline__ QuantDiv quant_div(float s) {
   return d;
 }
 
-// Two FP32 values as one 64-bit register pair, and back (the operand form of
-// Blackwell's packed f32x2 arithmetic).
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-  uint64_t v;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
-  return v;
-}
-__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
 // RN(x / s) for two elements of a block whose s passed quant_div's range
 // test: q0 = RN(x*r + RN(x*r')) (faithful), e = x - s*q0 (exact), q1 =
 // RN(q0 + e*r) (correctly rounded), each step one packed f32x2 operation

@@ -17,6 +17,7 @@
 #include "gemm_skinny.cuh"
 #include "gemm_tn.cuh"
 #include "gemm_tn2.cuh"
+#include "gemm_tn2b.cuh"
 #include "quant.cuh"
 #include "tcgemm.h"
 
@@ -318,13 +319,15 @@ tcg_status launch_tn_inst(const CUtensorMap& ma, const CUtensorMap& mb, const Ge
 }
 
 // Kernel choice for the dense path: the CTA-pair kernel for problems with at
-// least one full 256 x 256 tile, else the one-SM kernel.  TCG_KERNEL=1cta or
-// 2cta in the environment forces one of them (for tests and measurements).
+// least one full 256 x 256 tile, else the one-SM kernel; for block-scaled FP8,
+// the pair kernel for M > 128, else the skinny one.  TCG_KERNEL=1cta, 2cta or
+// skinny in the environment forces one of them (for tests and measurements).
 int forced_kernel() {
   const char* e = std::getenv("TCG_KERNEL");
   if (!e) return 0;
   if (std::strcmp(e, "1cta") == 0) return 1;
   if (std::strcmp(e, "2cta") == 0) return 2;
+  if (std::strcmp(e, "skinny") == 0) return 3;
   return 0;
 }
 
@@ -339,21 +342,21 @@ tcg_status launch_tn2_inst(const CUtensorMap& ma, const CUtensorMap& mb, const G
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
 
-// The persistent 256 x 256 pair-tile kernel.
-template <int kIn>
-tcg_status launch_tn2(const Common& a, const float* a_scale, const float* b_scale,
-                      cudaStream_t stream, int dev, int sms) {
-  const int in_bytes = kIn == 0 ? 2 : 1;
+// Tensor maps and the persistent schedule of the 256 x 256 pair-tile kernels:
+// whole tiles in waves of SMs/2 clusters, the rest split into two 256 x 128
+// halves when that still fits one wave.  Returns the grid (CTAs).
+tcg_status pair_setup(const Common& a, int in_bytes, int sms, CUtensorMap* ma, CUtensorMap* mb,
+                      Gemm2Params* pp, int* grid) {
   const CUtensorMapDataType dt =
-      kIn == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+      in_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint32_t box_k = kBKBytes / in_bytes;
-  CUtensorMap ma, mb;
-  if (tcg_status s = tensor_map(&ma, dt, a.A, a.K, a.M, a.lda * in_bytes, box_k, 128); s != TCG_OK)
+  if (tcg_status s = tensor_map(ma, dt, a.A, a.K, a.M, a.lda * in_bytes, box_k, 128); s != TCG_OK)
     return s;
-  if (tcg_status s = tensor_map(&mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, box_k, kBBoxRows);
+  if (tcg_status s = tensor_map(mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, box_k, kBBoxRows);
       s != TCG_OK)
     return s;
-  Gemm2Params p{};
+  Gemm2Params& p = *pp;
+  p = Gemm2Params{};
   p.M = (int32_t)a.M;
   p.N = (int32_t)a.N;
   p.K = (int32_t)a.K;
@@ -364,10 +367,9 @@ tcg_status launch_tn2(const Common& a, const float* a_scale, const float* b_scal
   if (tiles > INT32_MAX) return TCG_ERR_UNSUPPORTED;
   p.num_tiles = (int32_t)tiles;
   const int clusters_max = sms / 2;
-  int clusters;
+  int clusters = clusters_max;
   int64_t rest;
   if (tiles >= clusters_max) {
-    clusters = clusters_max;
     p.dp_waves = (int32_t)(tiles / clusters_max);
     rest = tiles % clusters_max;
   } else {
@@ -384,16 +386,56 @@ tcg_status launch_tn2(const Common& a, const float* a_scale, const float* b_scal
   p.ldd = a.ldd;
   p.alpha = a.alpha;
   p.beta = a.beta;
-  p.a_scale = a_scale;
   p.fp8_fmt = fp8_fmt_bits(a.a_fp8, a.b_fp8);
+  *grid = 2 * clusters;
+  return TCG_OK;
+}
+
+// The persistent 256 x 256 pair-tile kernel.
+template <int kIn>
+tcg_status launch_tn2(const Common& a, const float* a_scale, const float* b_scale,
+                      cudaStream_t stream, int dev, int sms) {
+  CUtensorMap ma, mb;
+  Gemm2Params p;
+  int grid;
+  if (tcg_status s = pair_setup(a, kIn == 0 ? 2 : 1, sms, &ma, &mb, &p, &grid); s != TCG_OK)
+    return s;
+  p.a_scale = a_scale;
   p.b_scale = b_scale;
-  const int grid = 2 * clusters;
   const bool has_c = a.beta != 0.0f;
   if (a.out == TCG_OUT_BF16)
     return has_c ? launch_tn2_inst<kIn, 0, true>(ma, mb, p, grid, dev, stream)
                  : launch_tn2_inst<kIn, 0, false>(ma, mb, p, grid, dev, stream);
   return has_c ? launch_tn2_inst<kIn, 1, true>(ma, mb, p, grid, dev, stream)
                : launch_tn2_inst<kIn, 1, false>(ma, mb, p, grid, dev, stream);
+}
+
+template <int kOut, bool kHasC>
+tcg_status launch_block_pair_inst(const CUtensorMap& ma, const CUtensorMap& mb,
+                                  const Gemm2Params& p, int grid, int dev, cudaStream_t stream) {
+  auto* fn = &gemm_fp8_block_pair_kernel<kOut, kHasC>;
+  if (tcg_status s = ensure_smem(fn, kP2SmemBytes, dev); s != TCG_OK) return s;
+  if (launch_gemm_kernel(fn, grid, kPbThreads, kP2SmemBytes, stream, 2, ma, mb, p) != cudaSuccess)
+    return TCG_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+// Block-scaled FP8 on 256 x 256 pair tiles (the schedule of launch_tn2).
+tcg_status launch_block_pair(const Common& a, const float* a_scale, const float* b_scale,
+                             cudaStream_t stream, int dev, int sms) {
+  CUtensorMap ma, mb;
+  Gemm2Params p;
+  int grid;
+  if (tcg_status s = pair_setup(a, 1, sms, &ma, &mb, &p, &grid); s != TCG_OK) return s;
+  p.a_scale = a_scale;
+  p.b_scale = b_scale;
+  const bool has_c = a.beta != 0.0f;
+  if (a.out == TCG_OUT_BF16)
+    return has_c ? launch_block_pair_inst<0, true>(ma, mb, p, grid, dev, stream)
+                 : launch_block_pair_inst<0, false>(ma, mb, p, grid, dev, stream);
+  return has_c ? launch_block_pair_inst<1, true>(ma, mb, p, grid, dev, stream)
+               : launch_block_pair_inst<1, false>(ma, mb, p, grid, dev, stream);
 }
 
 // The persistent 128 x 256 tile kernel (BF16, or per-tensor FP8).
@@ -660,7 +702,15 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   if (K == 0) return launch_k0(a, st);
   if (!a_scale || !b_scale) return TCG_ERR_INVALID_ARG;
   if (mode == TCG_SCALE_TENSOR) return launch_tn<1>(a, a_scale, b_scale, st);
-  return launch_skinny(a, a_scale, b_scale, st);  // any M: M > 128 in 128-row chunks
+  // Block scales: M <= 128 on the swap-AB skinny kernel, larger M on pair
+  // tiles (the skinny kernel also takes any M, in 128-row chunks).
+  const int fk = forced_kernel();
+  if (fk == 2 || (fk != 3 && M > 128)) {
+    int dev, sms;
+    if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+    return launch_block_pair(a, a_scale, b_scale, st, dev, sms);
+  }
+  return launch_skinny(a, a_scale, b_scale, st);
 }
 
 tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,

@@ -229,11 +229,15 @@ def test_fp8_block_skinny_shapes(M, N, K, out, beta):
     check_full(w, run(w))
 
 
-@pytest.mark.parametrize("M,N,K", [(5, 260, 300), (64, 1024, 4096), (128, 2048, 2048),
-                                   (20, 8192, 640), (300, 260, 384), (256, 4096, 512)])
-def test_fp8_block_scale_indexing_bit_exact(M, N, K):
+@pytest.mark.parametrize("M,N,K,kernel", [
+    (5, 260, 300, None), (64, 1024, 4096, None), (128, 2048, 2048, None), (20, 8192, 640, None),
+    (300, 260, 384, "2cta"), (256, 4096, 512, "2cta"), (520, 2300, 1100, "2cta"),
+    (300, 260, 384, "skinny"), (256, 4096, 512, "skinny")])
+def test_fp8_block_scale_indexing_bit_exact(monkeypatch, M, N, K, kernel):
     """Power-of-two block scales that depend on (row, K block) and (N block,
     K block) with small-integer codes: every misplaced scale changes bits."""
+    if kernel:
+        monkeypatch.setenv("TCG_KERNEL", kernel)
     KB, NB = (K + 127) // 128, (N + 127) // 128
     rng = np.random.default_rng(M + N)
     ints = np.array([-3, -2, -1, 0, 1, 2, 3], np.float32)
@@ -252,12 +256,17 @@ def test_fp8_block_scale_indexing_bit_exact(M, N, K):
     assert np.array_equal(d_to_host(run(w)).astype(np.float64), v)
 
 
-# M > 128: A in chunks of 128 rows, each tile a 128 x 128 block of D (the
-# general split, the cluster pair at 64 tiles, unsplit tiles at 128 tiles).
+# M > 128, on both kernels that take it: the pair-tile kernel (256 x 256
+# tiles; halves at the tail; whole waves plus a split tail at 2560 x 2048) and
+# the skinny kernel with A in chunks of 128 rows (the general split, the
+# cluster pair at 64 tiles, unsplit tiles at 128 tiles).
+@pytest.mark.parametrize("kernel", ["2cta", "skinny"])
 @pytest.mark.parametrize("M,N,K", [(129, 256, 512), (300, 1000, 1024), (256, 4096, 512),
-                                   (1024, 2048, 1536), (777, 3000, 2200)])
+                                   (1024, 2048, 1536), (777, 3000, 2200), (2560, 2048, 512),
+                                   (513, 130, 4100)])
 @pytest.mark.parametrize("out,beta", [("f32", 0.0), ("bf16", 1.0)])
-def test_fp8_block_scaled_large_m(M, N, K, out, beta):
+def test_fp8_block_scaled_large_m(monkeypatch, kernel, M, N, K, out, beta):
+    monkeypatch.setenv("TCG_KERNEL", kernel)
     w = fp8_case(M, N, K, seed=M + 3 * N + K, mode="block", out=out, beta=beta, outliers=0.01)
     check_full(w, run(w))
 
@@ -277,7 +286,7 @@ def test_fp8_block_scaled_4096_cubed_sampled():
     _sampled(w, out="bf16")
 
 
-@pytest.mark.parametrize("M,N", [(64, 4096), (16, 8192), (600, 2048)])
+@pytest.mark.parametrize("M,N", [(64, 4096), (16, 8192), (600, 2048), (4096, 4096)])
 def test_fp8_block_skinny_deterministic(M, N):
     w = fp8_case(M, N, 4096, seed=11, mode="block", out="f32", outliers=0.01)
     d1 = d_to_host(run(w))
@@ -407,6 +416,13 @@ def test_fp8_e5m2_block_scaled_skinny(a_fmt, b_fmt, M, N, K):
 
 
 @pytest.mark.parametrize("a_fmt,b_fmt", FMTS)
+@pytest.mark.parametrize("M,N,K", [(300, 700, 1000), (1024, 1024, 2048)])
+def test_fp8_e5m2_block_scaled_pair(a_fmt, b_fmt, M, N, K):
+    w = fp8_fmt_case(M, N, K, 7 * M + N, "block", a_fmt, b_fmt)
+    check_full(w, run(w))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", FMTS)
 def test_fp8_e5m2_small_integers_bit_exact(a_fmt, b_fmt):
     """Small integers (exact in both encodings) with power-of-two scales: the
     FP32 accumulation is exact, so a format mix-up changes bits."""
@@ -437,7 +453,7 @@ def test_fp8_e5m2_small_integers_bit_exact(a_fmt, b_fmt):
 # ------------------------------------------------------------- guard bands
 
 @pytest.mark.parametrize("case", ["bf16_1cta", "bf16_2cta", "fp8_tensor", "fp8_block",
-                                  "fp8_block_pair"])
+                                  "fp8_block_pair", "fp8_block_large_m"])
 def test_output_guard_bands_untouched(monkeypatch, case):
     """D is a view into a larger buffer filled with a sentinel: the kernels
     write exactly the M x N view (no row, column or padding outside it)."""
@@ -448,6 +464,8 @@ def test_output_guard_bands_untouched(monkeypatch, case):
         w = fp8_case(300, 260, 128, seed=52, mode="tensor", out="bf16")
     elif case == "fp8_block":
         w = fp8_case(20, 300, 256, seed=53, mode="block", out="f32")
+    elif case == "fp8_block_large_m":
+        w = fp8_case(300, 260, 384, seed=55, mode="block", out="bf16", beta=1.0)
     else:
         w = fp8_case(100, 8192, 256, seed=54, mode="block", out="bf16")
     dt = torch.float32 if w.out == "f32" else torch.bfloat16
