@@ -64,7 +64,7 @@ class Workload:
 
 
 NAMES = ("bf16_256", "bf16_4096", "fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64",
-         "fp8_skinny_128")
+         "fp8_skinny_128", "fp8_block_4096")
 
 
 def make(name: str, *, M=None, N=None, K=None) -> Workload:
@@ -94,6 +94,13 @@ def make(name: str, *, M=None, N=None, K=None) -> Workload:
         w.A = bf16(4, 1, M, K)
         w.B = bf16(4, 2, N, K, p1=0.02)
         w.C = bf16(4, 3, M, N)
+        return w
+    if name == "fp8_block_4096":
+        # the block scaling of the skinny workload on a square 4096^3 problem
+        M, N, K = M or 4096, N or 4096, K or 4096
+        w = Workload(name, M, N, K, "fp8_block", "bf16")
+        w.A, w.a_scale = e4m3_rowblock(values_f32(6, 1, M, K, out_prob=0.01, out_factor=50.0))
+        w.B, w.b_scale = e4m3_block128(values_f32(6, 2, N, K, out_prob=0.01, out_factor=50.0))
         return w
     if name.startswith("fp8_skinny_"):
         M = M or int(name.rsplit("_", 1)[1])

@@ -702,10 +702,20 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   if (K == 0) return launch_k0(a, st);
   if (!a_scale || !b_scale) return TCG_ERR_INVALID_ARG;
   if (mode == TCG_SCALE_TENSOR) return launch_tn<1>(a, a_scale, b_scale, st);
-  // Block scales: M <= 128 on the swap-AB skinny kernel, larger M on pair
-  // tiles (the skinny kernel also takes any M, in 128-row chunks).
+  // Block scales: M <= 128 on the swap-AB skinny kernel; larger M on pair
+  // tiles when their work units (256 x 256 tiles, or halves of them when few)
+  // keep at least half the SMs busy, else on the skinny kernel with A in
+  // 128-row chunks (more, smaller tiles).
   const int fk = forced_kernel();
-  if (fk == 2 || (fk != 3 && M > 128)) {
+  if (fk != 3 && M > 128) {
+    int dev, sms;
+    if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+    const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    const int64_t clusters = sms / 2;
+    const int64_t units = tiles >= clusters ? tiles : (tiles * 2 <= clusters ? tiles * 2 : tiles);
+    if (fk == 2 || units * 2 >= sms / 2)
+      return launch_block_pair(a, a_scale, b_scale, st, dev, sms);
+  } else if (fk == 2) {
     int dev, sms;
     if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
     return launch_block_pair(a, a_scale, b_scale, st, dev, sms);
