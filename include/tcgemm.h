@@ -99,9 +99,13 @@ tcg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
  *                    scales sa[i,kb] * sb[j/128,kb] ("promotion": partial sums
  *                    moved to FP32 at intervals, "Tensor Cores: Matrix
  *                    Instructions, Swizzling and FP8, Measured", Step 5).
- *                    Any M: the kernel is built for M <= 128 (the skinny,
- *                    decode-sized shape, one chunk of A); larger M runs in
- *                    chunks of 128 rows of A, each output tile 128 x 128.
+ *                    Any M: M <= 128 (the skinny, decode-sized shape) runs
+ *                    swap-AB with A in one chunk; larger M runs on 256 x 256
+ *                    CTA-pair tiles, or, when those would leave more than
+ *                    half the SMs idle, in chunks of 128 rows of A (128 x 128
+ *                    output tiles).  The result does not depend on the
+ *                    choice beyond FP32 rounding order, and repeats bit for
+ *                    bit for the same call.
  */
 tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                          const void* B, int64_t ldb, const float* a_scale, const float* b_scale,

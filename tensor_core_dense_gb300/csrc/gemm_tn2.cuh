@@ -306,10 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
         tmem_ld_wait(r);
         if (c == nchunks - 1) {
-          // hand the accumulator back to the leader's MMA warp
+          // hand the accumulator back to the leader's MMA warp (ordered by
+          // the tcgen05 fence; a CTA-scope release does not wait for this
+          // thread's earlier D stores)
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(map_shared_to_cta(tempty_bar(acc), 0));
+          if (lane == 0) mbar_arrive_remote_cta(map_shared_to_cta(tempty_bar(acc), 0));
         }
         float a[32];
 #pragma unroll

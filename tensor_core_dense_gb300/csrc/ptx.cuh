@@ -390,12 +390,6 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on an mbarrier that may live in another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
 // Arrive on an mbarrier in another CTA of the cluster with CTA-scope release:
 // for hand-backs whose ordering comes from a tcgen05 fence (a drained TMEM
 // buffer), so the arrive does not wait for this thread's outstanding global
