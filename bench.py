@@ -149,6 +149,64 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, read-only queries) every `ms` milliseconds on a thread, only
+    while started: sized for timed regions of a few milliseconds, which an
+    nvidia-smi process started beside the run cannot resolve.  Rows have the
+    ClockSampler layout."""
+
+    SW_POWER_CAP, HW_SLOWDOWN, SW_THERMAL, HW_THERMAL = 0x4, 0x8, 0x20, 0x40
+
+    def __init__(self, device_uuid: str, ms: float = 1.0):
+        import ctypes
+        self.ms = ms
+        self.rows = []
+        self.thread = None
+        self.running = False
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(device_uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for " + device_uuid)
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # 1 = NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+
+    def _sample(self):
+        import ctypes
+        c, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+        self.reasons_fn(self.h, ctypes.byref(rs))
+        act = lambda bit: "Active" if rs.value & bit else "Not Active"  # noqa: E731
+        self.rows.append(dict(sm=float(c.value), max=self.max_mhz, power=pw.value / 1000.0,
+                              hw=act(self.HW_SLOWDOWN), hw_thermal=act(self.HW_THERMAL),
+                              sw_thermal=act(self.SW_THERMAL), sw_power=act(self.SW_POWER_CAP)))
+
+    def _loop(self):
+        while self.running:
+            self._sample()
+            time.sleep(self.ms / 1000.0)
+
+    def start(self):
+        import threading
+        self.running = True
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.running = False
+        if self.thread is not None:
+            self.thread.join()
+        self._sample()  # at least one sample, taken right at the end of the region
+        return self.rows
+
+
 # -------------------------------------------------------------- our path
 
 def _dist_init(args):
@@ -268,9 +326,10 @@ class Rotation:
                 f"finds its operands in L2")
 
 
-def time_graph(rot, steps, warmup):
+def time_graph(rot, steps, warmup, sampler=None):
     """Time `steps` back-to-back calls (cycling the copies) replayed from one
-    CUDA graph; returns (total ms, kernel launches inside the graph)."""
+    CUDA graph; returns (total ms, kernel launches inside the graph).  A
+    sampler (start/stop) runs exactly around the timed replay."""
     import torch
 
     import tensor_core_dense_gb300 as tcg
@@ -289,10 +348,14 @@ def time_graph(rot, steps, warmup):
     g.replay()  # one untimed replay
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler is not None:
+        sampler.start()
     e0.record()
     g.replay()
     e1.record()
     torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.stop()
     return e0.elapsed_time(e1), launches, g
 
 
@@ -426,13 +489,21 @@ def run_ours(args):
 
     dev_uuid = str(torch.cuda.get_device_properties(local).uuid)
     smi_id = dev_uuid if dev_uuid.startswith("GPU-") else f"GPU-{dev_uuid}"
-    sampler = ClockSampler(smi_id)
+    # clocks during the timed replay: NVML polled every millisecond (the
+    # region lasts milliseconds), else nvidia-smi around the whole run
+    try:
+        nvml = NvmlSampler(smi_id)
+        sampler = None
+    except (OSError, AttributeError):
+        nvml = None
+        sampler = ClockSampler(smi_id)
     # W warm-up steps, capture of the K timed steps, then the timed replay
     # (barrier + synchronize on both sides inside time_graph's sync points)
     _barrier(world)
-    total_ms, launches, graph = time_graph(rot, args.steps, args.warmup)
+    total_ms, launches, graph = time_graph(rot, args.steps, args.warmup, nvml)
     _barrier(world)
-    clocks = ClockSampler.summary(sampler.stop())
+    clocks = ClockSampler.summary(nvml.rows if nvml is not None else sampler.stop())
+    clocks["source"] = "nvml, 1 ms, timed replay only" if nvml is not None else "nvidia-smi, 50 ms"
     assert tcg.last_device_status() == tcg.OK
     del graph
 
