@@ -410,11 +410,11 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
             tmem_base + ((q * 32u) << 16) + b * kMp + (uint32_t)(col0 + c1), r);
 #pragma unroll
         for (int c = 0; c < kPiece; c += 4) {
+          // acc += partial * scale product, two columns per packed f32x2 FMA
+          // (each lane rounded as fmaf)
           const float4 s4 = *reinterpret_cast<const float4*>(sc + c1 + c);
-          acc[c1 + c + 0] = fmaf(__uint_as_float(r[c + 0]), s4.x, acc[c1 + c + 0]);
-          acc[c1 + c + 1] = fmaf(__uint_as_float(r[c + 1]), s4.y, acc[c1 + c + 1]);
-          acc[c1 + c + 2] = fmaf(__uint_as_float(r[c + 2]), s4.z, acc[c1 + c + 2]);
-          acc[c1 + c + 3] = fmaf(__uint_as_float(r[c + 3]), s4.w, acc[c1 + c + 3]);
+          fma_f32x2_pair(acc[c1 + c + 0], acc[c1 + c + 1], r[c + 0], r[c + 1], s4.x, s4.y);
+          fma_f32x2_pair(acc[c1 + c + 2], acc[c1 + c + 3], r[c + 2], r[c + 3], s4.z, s4.w);
         }
       }
       tc_fence_before_sync();

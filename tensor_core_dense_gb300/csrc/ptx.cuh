@@ -327,6 +327,17 @@ __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
+// (a0, a1) += (p0, p1) * (s0, s1) in one packed instruction (p0, p1: FP32 bit
+// patterns); each lane is rounded exactly as a scalar fmaf.
+__device__ __forceinline__ void fma_f32x2_pair(float& a0, float& a1, uint32_t p0, uint32_t p1,
+                                               float s0, float s1) {
+  uint64_t pp, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "r"(p0), "r"(p1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pp), "l"(pack_f32x2(s0, s1)),
+      "l"(pack_f32x2(a0, a1)));
+  unpack_f32x2(d, a0, a1);
+}
+
 // acc += (p0, p1) * s2 on a packed pair (p0, p1: FP32 bit patterns, e.g. two
 // TMEM columns); each lane is rounded exactly as a scalar fmaf.
 __device__ __forceinline__ void fma_f32x2_acc(uint64_t& acc, uint32_t p0, uint32_t p1,
