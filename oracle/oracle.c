@@ -42,8 +42,9 @@
  * then multiplied by the block's FP64 scale product s_a * s_b (exact, 24+24
  * bits).  With E5M2 operands (exponents 2^-16 .. 2^15) a block sum can span
  * more than 53 bits and is exact only up to FP64 rounding, at most
- * 128 * 2^-53 of the block's sum of |products|.  The sum of |a_ik * b_kj| is returned beside each value as the
- * error bound the tolerances are stated against.
+ * 128 * 2^-53 of the block's sum of |products|.  The sum of |a_ik * b_kj| is
+ * returned beside each value as the error bound the tolerances are stated
+ * against.
  *
  * The scale layouts for the 128-block mode (the pages name block scaling but
  * give no storage order; this is the library's choice, stated here and in

@@ -26,13 +26,16 @@
 // blocks of B's scales; the warps of column half h use block 2*tn + h.  The
 // scales come in sets of kPbAhead K blocks: a set is loaded into registers
 // one set ahead of use, so a load has kPbAhead K blocks of MMA time to land
-// before anything reads its register.  After the tile's last K block the same warps apply alpha and
-// beta*C, convert and store; the MMA meanwhile fills both buffers with the
-// next tile's first K blocks.
+// before anything reads its register.  After the tile's last K block the same
+// warps apply alpha and beta*C, convert and store; the MMA meanwhile fills
+// both buffers with the next tile's first K blocks.
 //
 // Barriers as in gemm_tn2.cuh, except that tfull/tempty turn over once per K
 // block instead of once per tile; tempty[a] counts 16 arrivals (8 warps in
-// each CTA).
+// each CTA), each a CTA-scope release arrive after a tcgen05 fence.  With two
+// buffers the MMA of block g+2 waits for both CTAs' promotion of block g, so
+// a K block costs about half of (MMA + promotion + the two notification
+// latencies); a 256-column partial per buffer leaves no room for a third.
 #pragma once
 
 #include <cuda.h>

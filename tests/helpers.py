@@ -93,7 +93,8 @@ def to_device(arr, dtype=None):
     if arr is None:
         return None
     if arr.dtype == np.uint16:
-        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).cuda().view(torch.bfloat16)
+        t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16))
+        return t.cuda().view(torch.bfloat16)
     return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
 
 

@@ -381,8 +381,9 @@ def fp8_fmt_case(M, N, K, seed, mode, a_fmt, b_fmt, out="f32", beta=0.0):
         kb = np.arange(K) // 128
         sa2 = np.stack([np.abs(xa[:, kb == j]).max(1) for j in range(KB)]) / top[a_fmt]  # KB x M
         sb2 = np.array([[np.abs(xb[n * 128:(n + 1) * 128][:, kb == j]).max() for j in range(KB)]
-                        for n in range(NB)]) / top[b_fmt]                                     # NB x KB
-        sa2, sb2 = np.maximum(sa2, 1e-30).astype(np.float32), np.maximum(sb2, 1e-30).astype(np.float32)
+                        for n in range(NB)]) / top[b_fmt]  # NB x KB
+        sa2 = np.maximum(sa2, 1e-30).astype(np.float32)
+        sb2 = np.maximum(sb2, 1e-30).astype(np.float32)
         w.A = cast(xa, a_fmt, sa2.T[:, kb])
         w.B = cast(xb, b_fmt, np.repeat(sb2, 128, axis=0)[:N][:, kb])
         sa, sb = sa2.ravel(), sb2.ravel()

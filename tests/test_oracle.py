@@ -160,7 +160,8 @@ def test_e4m3_encode_matches_torch_and_the_input_generator():
 
 def test_bf16_decode_matches_torch_for_all_patterns():
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
-    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    ref = ref.to(torch.float64).numpy()
     got = oracle.bf16_decode(bits)
     nan = np.isnan(ref)
     assert np.array_equal(nan, np.isnan(got))
@@ -293,7 +294,8 @@ def test_fp8_block_scale_indexing_exact():
 def test_fp8_tensor_scale_exact():
     M, N, K = 4, 6, 64
     rng = np.random.default_rng(8)
-    qa = rng.integers(0, 0x77, size=(M, K)).astype(np.uint8) | (rng.integers(0, 2, (M, K)) << 7).astype(np.uint8)
+    qa = (rng.integers(0, 0x77, size=(M, K)).astype(np.uint8)
+          | (rng.integers(0, 2, (M, K)) << 7).astype(np.uint8))
     qb = rng.integers(0, 0x77, size=(N, K)).astype(np.uint8)
     sa, sb = np.array([2.0 ** -3], np.float32), np.array([2.0 ** 5], np.float32)
     v, _ = oracle.gemm(M, N, K, qa, K, qb, K, in_type=oracle.IN_E4M3,
