@@ -507,6 +507,25 @@ def test_bf16_output_beyond_2_31_elements():
     torch.cuda.empty_cache()
 
 
+def test_fp8_block_pair_output_beyond_2_31_elements():
+    """Block-scaled FP8 on the pair-tile kernel with a 65,600 x 32,768 output
+    (2.15e9 elements, 4.3 GB of BF16) and a ragged last tile row: output and
+    scale offsets past 2^31, checked on the corner tiles."""
+    M, N, K = 65600, 32768, 256
+    w = fp8_case(M, N, K, seed=63, mode="block", out="bf16", outliers=0.01)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    run(w, D=D)
+    torch.cuda.synchronize()
+    tiles = [(0, 0, 128, 128), (M - 128, N - 128, 128, 128), (M - 64, 0, 64, 128),
+             (0, N - 128, 128, 128), (40000, 20000, 128, 128)]
+    vs, bs = oracle_for(w, tiles=tiles)
+    for (i0, j0, mi, nj), v, b in zip(tiles, vs, bs):
+        got = D[i0:i0 + mi, j0:j0 + nj].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        check_bf16("fp8", got, v, b, what=f"huge block {i0},{j0}")
+    del D
+    torch.cuda.empty_cache()
+
+
 def test_fp8_block_skinny_a_million_columns():
     """N = 1,000,000 (7,813 N tiles, more than the SMs: the general stream-K
     spread with the global workspace), ragged last tile."""
