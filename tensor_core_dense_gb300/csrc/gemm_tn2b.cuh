@@ -21,8 +21,11 @@
 // two 256-column TMEM buffers, alternating.  Eight promotion warps, two per
 // TMEM lane quarter (warp w reads lanes 32*(w%4)..), each own 128 columns of
 // the CTA's 128 x 256 accumulator as FP32 registers: they load the partial
-// (tcgen05.ld), add partial * sa[row, kb] * sb[column block, kb] with packed
-// f32x2 FMAs, and hand the buffer back.  A 256-column tile spans two column
+// (tcgen05.ld), add partial * sa[row, kb] * sb[column block, kb] with scalar
+// FMAs, and hand the buffer back.  (FP32 work on the SM slows the tensor
+// pipe: without the FMAs a K block's MMA completes in about 730 cycles, with
+// them about 1170.  Packed f32x2 FMAs, half the instructions, were 1-2 %
+// slower than scalar ones.)  A 256-column tile spans two column
 // blocks of B's scales; the warps of column half h use block 2*tn + h.  The
 // scales come in sets of kPbAhead K blocks: a set is loaded into registers
 // one set ahead of use, so a load has kPbAhead K blocks of MMA time to land
@@ -313,9 +316,9 @@ __global__ void __launch_bounds__(kPbThreads, 1)
       const int ncols = nsub / 2;  // this warp's columns: 128, or 64 for a half tile
       const int row = tm * 256 + row_in_tile;
       const int col0 = tn * 256 + w.sub * nsub + h * ncols;
-      uint64_t acc[64];  // 128 FP32 sums as packed pairs (operands of fma.rn.f32x2)
+      float acc[128];  // this thread's row, this warp's 128 (or 64) columns
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc[j] = 0ull;
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
         const uint32_t buf = g & 1u, ph = (g >> 1) & 1u;
         const uint32_t slot = g % kPbAhead;
@@ -341,7 +344,6 @@ __global__ void __launch_bounds__(kPbThreads, 1)
           }
         }
         const float sk = sa_k * sb_k;
-        const uint64_t s2 = pack_f32x2(sk, sk);
         uint32_t got = 0;
         if (lane == 0) got = wait_phase(tfull_bar(buf), ph, abort_flag, 0x34) ? 1u : 0u;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
@@ -359,8 +361,8 @@ __global__ void __launch_bounds__(kPbThreads, 1)
             pb_tmem_ld(t_row + (uint32_t)(c * kPbChunk), r);
             tmem_ld_wait_n(r);
 #pragma unroll
-            for (int j = 0; j < kPbChunk / 2; ++j)
-              fma_f32x2_acc(acc[c * (kPbChunk / 2) + j], r[2 * j], r[2 * j + 1], s2);
+            for (int j = 0; j < kPbChunk; ++j)
+              acc[c * kPbChunk + j] = fmaf(__uint_as_float(r[j]), sk, acc[c * kPbChunk + j]);
           }
         }
         // hand the buffer back to the leader's MMA warp (ordered by the
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kPbThreads, 1)
         if (c * 32 < ncols) {
           float a[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) unpack_f32x2(acc[c * 16 + j], a[2 * j], a[2 * j + 1]);
+          for (int j = 0; j < 32; ++j) a[j] = acc[c * 32 + j];
           store_row_chunk2<kOut, kHasC>(p, row, col0 + c * 32, a, p.alpha);
         }
       }

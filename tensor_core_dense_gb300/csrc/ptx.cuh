@@ -338,15 +338,6 @@ __device__ __forceinline__ void fma_f32x2_pair(float& a0, float& a1, uint32_t p0
   unpack_f32x2(d, a0, a1);
 }
 
-// acc += (p0, p1) * s2 on a packed pair (p0, p1: FP32 bit patterns, e.g. two
-// TMEM columns); each lane is rounded exactly as a scalar fmaf.
-__device__ __forceinline__ void fma_f32x2_acc(uint64_t& acc, uint32_t p0, uint32_t p1,
-                                              uint64_t s2) {
-  uint64_t pp;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "r"(p0), "r"(p1));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(pp), "l"(s2));
-}
-
 // Two FP32 -> packed BF16x2, round to nearest even (lo in bits 0-15).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;
