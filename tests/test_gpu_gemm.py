@@ -507,6 +507,53 @@ def test_bf16_output_beyond_2_31_elements():
     torch.cuda.empty_cache()
 
 
+# D = alpha*A*B + beta*D in place (C and D the same array, which the ABI
+# allows when ldc == ldd): every kernel reads an output's C value in the thread
+# that then writes it, once.
+@pytest.mark.parametrize("case", ["bf16_1cta", "bf16_2cta", "fp8_tensor", "fp8_skinny",
+                                  "fp8_skinny_split", "fp8_block_pair", "k0"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_d_aliases_c_in_place(monkeypatch, case, out):
+    if case.startswith("bf16"):
+        monkeypatch.setenv("TCG_KERNEL", case.split("_")[1])
+        w = bf16_case(300, 520, 200, seed=71, out=out, alpha=0.5, beta=-1.5)
+    elif case == "fp8_tensor":
+        w = fp8_case(300, 520, 256, seed=72, mode="tensor", out=out, beta=2.0)
+    elif case == "fp8_skinny":
+        w = fp8_case(40, 8192, 512, seed=73, mode="block", out=out, beta=1.0)
+    elif case == "fp8_skinny_split":
+        w = fp8_case(64, 1000, 4096, seed=74, mode="block", out=out, beta=1.0)
+    elif case == "fp8_block_pair":
+        w = fp8_case(600, 1000, 1024, seed=75, mode="block", out=out, beta=-0.75)
+    else:
+        w = bf16_case(100, 72, 0, seed=76, out=out, beta=3.0)
+        w.A = np.zeros((100, 8), np.uint16)
+        w.B = np.zeros((72, 8), np.uint16)
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    step = 8 if out == "bf16" else 4
+    D = torch.empty((w.M, _pad(w.N, step)), dtype=dt, device="cuda")[:, :w.N]
+    cdev = to_device(w.C)
+    D.copy_(cdev[:, :w.N].to(dt))
+    import tensor_core_dense_gb300 as tcg
+    A, B = to_device(w.A), to_device(w.B)
+    if w.kind == "bf16":
+        tcg.gemm_bf16(A[:, :w.K], B[:, :w.K], D, D, alpha=w.alpha, beta=w.beta)
+    else:
+        mode = tcg.SCALE_TENSOR if w.kind == "fp8_tensor" else tcg.SCALE_BLOCK128
+        tcg.gemm_fp8_e4m3(A[:, :w.K], B[:, :w.K], to_device(w.a_scale), to_device(w.b_scale), D,
+                          D, mode=mode, alpha=w.alpha, beta=w.beta)
+    if w.K == 0:
+        got = d_to_host(D)
+        c = c_values(w.C)[:, :w.N]
+        want = (np.float64(w.beta) * c).astype(np.float32)
+        if out == "bf16":
+            assert np.array_equal(got, synth.to_bf16(want)[:, :w.N])
+        else:
+            assert np.array_equal(got, want)
+        return
+    check_full(w, D)
+
+
 def test_fp8_block_pair_output_beyond_2_31_elements():
     """Block-scaled FP8 on the pair-tile kernel with a 65,600 x 32,768 output
     (2.15e9 elements, 4.3 GB of BF16) and a ragged last tile row: output and
