@@ -134,7 +134,7 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
 
 /*
  * gemm_fp8_e4m3_block_noalloc -- the TCG_SCALE_BLOCK128 case of gemm_fp8_e4m3
- * (M <= 128) without any device allocation.  The pages have no counterpart
+ * without any device allocation.  The pages have no counterpart
  * to this entry point; it exists for callers that cannot let a library call
  * cudaMalloc: code being recorded into a CUDA graph (an allocation during
  * stream capture breaks the capture), latency-bound loops that cannot absorb
@@ -142,19 +142,21 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  * whose own memory manager owns all of device memory.
  *
  * Arguments, layouts, alignment and numerics are those of gemm_fp8_e4m3 with
- * mode = TCG_SCALE_BLOCK128.  The split-K scratch is a fixed 32 MiB array
+ * mode = TCG_SCALE_BLOCK128.  M > 128 runs on the CTA-pair kernel, which
+ * needs no scratch.  For M <= 128 the split-K scratch is a fixed 32 MiB array
  * inside the library's device code, present on every device that loads the
  * library until the process exits; the caller still provides A, B, the
  * scales, C and D.  A problem whose scratch would exceed 32 MiB (counters:
  * ceil(N/128) words rounded up to 256 bytes; partial sums: two Mp x 128 FP32
  * tiles per CTA of the launch, at most 152 CTAs x 64 KB; Mp = M rounded up to
  * 16/32/64/128) is rejected with TCG_ERR_UNSUPPORTED before anything is
- * enqueued; M > 128 is rejected the same way.
+ * enqueued.
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and raises the kernel's shared-memory limit; make that
- * first call before any stream capture.  Each call clears the tile counters
- * (a memset on `stream`) and then launches one kernel.  All calls on a device
+ * first call before any stream capture.  Each call with M <= 128 clears the
+ * tile counters (a memset on `stream`) and then launches one kernel; M > 128
+ * launches one kernel.  All calls on a device
  * share the one array: calls whose executions overlap on the GPU (different
  * streams without ordering between them) race on it and give wrong results.
  */

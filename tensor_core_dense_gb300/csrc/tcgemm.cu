@@ -342,6 +342,8 @@ tcg_status launch_tn2_inst(const CUtensorMap& ma, const CUtensorMap& mb, const G
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
 
+tcg_status pair_schedule(const Common& a, int in_bytes, int sms, Gemm2Params* pp, int* grid);
+
 // Tensor maps and the persistent schedule of the 256 x 256 pair-tile kernels:
 // whole tiles in waves of SMs/2 clusters, the rest split into two 256 x 128
 // halves when that still fits one wave.  Returns the grid (CTAs).
@@ -355,6 +357,11 @@ tcg_status pair_setup(const Common& a, int in_bytes, int sms, CUtensorMap* ma, C
   if (tcg_status s = tensor_map(mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, box_k, kBBoxRows);
       s != TCG_OK)
     return s;
+  return pair_schedule(a, in_bytes, sms, pp, grid);
+}
+
+// The schedule part of pair_setup (no tensor maps, no host-side tables).
+tcg_status pair_schedule(const Common& a, int in_bytes, int sms, Gemm2Params* pp, int* grid) {
   Gemm2Params& p = *pp;
   p = Gemm2Params{};
   p.M = (int32_t)a.M;
@@ -941,6 +948,49 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
 
+// Block-scaled FP8 for M > 128 on the pair-tile kernel, which needs no
+// scratch: stack-encoded tensor maps, a per-device flag for the shared-memory
+// limit instead of the host-side table.
+template <int kOut, bool kHasC>
+tcg_status launch_block_pair_noalloc_inst(const Common& a, const float* sa, const float* sb,
+                                          cudaStream_t stream, int dev, int sms) {
+  CUtensorMap ma, mb;
+  if (tcg_status s = encode_map_uncached(&ma, a.A, a.K, a.M, a.lda, 128); s != TCG_OK) return s;
+  if (tcg_status s = encode_map_uncached(&mb, a.B, a.K, a.N, a.ldb, kBBoxRows); s != TCG_OK)
+    return s;
+  Gemm2Params p;
+  int grid;
+  if (tcg_status s = pair_schedule(a, 1, sms, &p, &grid); s != TCG_OK) return s;
+  p.a_scale = sa;
+  p.b_scale = sb;
+  auto* fn = &gemm_fp8_block_pair_kernel<kOut, kHasC>;
+  {
+    static bool raised[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!raised[dev]) {
+      if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kP2SmemBytes) != cudaSuccess)
+        return TCG_ERR_CUDA;
+      raised[dev] = true;
+    }
+  }
+  if (launch_gemm_kernel(fn, grid, kPbThreads, kP2SmemBytes, stream, 2, ma, mb, p) != cudaSuccess)
+    return TCG_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+tcg_status launch_block_pair_noalloc(const Common& a, const float* sa, const float* sb,
+                                     cudaStream_t stream, int dev, int sms) {
+  const bool has_c = a.beta != 0.0f;
+  if (a.out == TCG_OUT_BF16)
+    return has_c ? launch_block_pair_noalloc_inst<0, true>(a, sa, sb, stream, dev, sms)
+                 : launch_block_pair_noalloc_inst<0, false>(a, sa, sb, stream, dev, sms);
+  return has_c ? launch_block_pair_noalloc_inst<1, true>(a, sa, sb, stream, dev, sms)
+               : launch_block_pair_noalloc_inst<1, false>(a, sa, sb, stream, dev, sms);
+}
+
 }  // namespace
 }  // namespace tcg
 
@@ -956,9 +1006,9 @@ extern "C" tcg_status gemm_fp8_e4m3_block_noalloc(int64_t M, int64_t N, int64_t 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (K == 0) return launch_k0(a, st);
   if (!a_scale || !b_scale) return TCG_ERR_INVALID_ARG;
-  if (M > 128) return TCG_ERR_UNSUPPORTED;
   int dev, sms;
   if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+  if (M > 128) return launch_block_pair_noalloc(a, a_scale, b_scale, st, dev, sms);
   if (M <= 16) return launch_skinny_noalloc<16>(a, a_scale, b_scale, st, dev, sms);
   if (M <= 32) return launch_skinny_noalloc<32>(a, a_scale, b_scale, st, dev, sms);
   if (M <= 64) return launch_skinny_noalloc<64>(a, a_scale, b_scale, st, dev, sms);
