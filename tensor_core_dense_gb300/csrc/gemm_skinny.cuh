@@ -1,5 +1,6 @@
-// gemm_skinny.cuh -- FP8 GEMM with 128-block scales, swap-AB: skinny M (<= 128)
-// in one chunk, larger M in chunks of 128 rows.
+// gemm_skinny.cuh -- swap-AB GEMM for skinny M: FP8 with 128-block scales (M
+// <= 128 in one chunk, larger M in chunks of 128 rows), and for M <= 128 also
+// per-tensor FP8 and BF16 (one scale product for every step, or 1).
 //
 //   D[m, n] = alpha * sum_kb sa[kb*M + m] * sb[(n/128)*KB + kb]
 //                    * sum_{k in block kb} qa[m, k] * qb[n, k]   (+ beta * C)
@@ -99,7 +100,9 @@ struct SkinnyParams {
   float alpha, beta;
   int32_t out_f32, has_c;
   uint32_t fp8_fmt;  // UMMA A (= B, the weights) / UMMA B (= A) format fields
-  int32_t pad_;
+  // 1: one scale for the whole problem, a_scale[0] * b_scale[0] (per-tensor
+  // FP8; 1 when a pointer is null, as for BF16) instead of the block tables
+  int32_t scalar_scale;
   float* ws;               // [grid][2][Mp][128] partial sums: a CTA's first and last piece
   unsigned int* counters;  // [n_tiles * m_tiles], zero between calls
 };
@@ -177,19 +180,23 @@ __device__ __forceinline__ void emit_four(const SkinnyParams& p, int m, int n, f
 
 // kMChunks: M > 128, A in chunks of kMp = 128 rows.  Without it m_tiles is the
 // constant 1, so the chunk index folds away (M <= 128 keeps its lean code).
-template <int kMp, bool kPair, bool kMChunks>
+// kIn: 1 = FP8 (kind::f8f6f4, 128 K elements per step), 0 = BF16 (kind::f16,
+// 64 K elements per step: a step is 128 bytes of K either way).
+template <int kMp, bool kPair, bool kMChunks, int kIn = 1>
 __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     gemm_fp8_block_skinny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                  const __grid_constant__ CUtensorMap tmap_b,
                                  const SkinnyParams p) {
   using Cfg = SkinnyCfg<kMp>;
+  constexpr int kKElems = kIn == 1 ? 128 : 64;  // K elements per 128-byte step
   constexpr int S = Cfg::kStages;
   constexpr int kHalf = Cfg::kHalf;
   constexpr int kSkNumAcc = Cfg::kNumAcc;
   constexpr int kSkEpiThreads = Cfg::kEpiThreads;
   constexpr uint32_t kEpiWarps = Cfg::kEpiWarps;
-  // FP8 x FP8 -> F32, M=128, N=Mp; the operand formats come from p.fp8_fmt
-  const uint32_t kIdesc = make_idesc(0, 0, 128, kMp) | p.fp8_fmt;
+  // FP8 x FP8 (formats from p.fp8_fmt) or BF16 x BF16 -> F32, M=128, N=Mp
+  const uint32_t kIdesc =
+      kIn == 1 ? make_idesc(0, 0, 128, kMp) | p.fp8_fmt : make_idesc(1, 1, 128, kMp);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -274,8 +281,8 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
-        tma_load_2d_hint(b_smem(s), &tmap_b, full_bar(s), kb * 128, nt * 128, stream_policy);
-        tma_load_2d_hint(a_smem(s), &tmap_a, full_bar(s), kb * 128, mt * kMp, keep_policy);
+        tma_load_2d_hint(b_smem(s), &tmap_b, full_bar(s), kb * kKElems, nt * 128, stream_policy);
+        tma_load_2d_hint(a_smem(s), &tmap_a, full_bar(s), kb * kKElems, mt * kMp, keep_policy);
       }
       grid_launch_dependents();  // every load is issued: the next kernel may launch
       if (!ok) {
@@ -307,7 +314,12 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
         const uint64_t bd = smem_desc_k_sw128(a_smem(s));  // UMMA B: Mp rows of A
         const uint32_t d_tmem = tmem_base + b * kMp;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mma_e4m3(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, k != 0);
+        for (int k = 0; k < 4; ++k) {  // 32 bytes of K per instruction
+          if (kIn == 1)
+            mma_e4m3(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, k != 0);
+          else
+            mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, k != 0);
+        }
         issued = true;
         tc_commit(empty_bar(s));
         tc_commit(tfull_bar(b));
@@ -373,8 +385,13 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
               sk_tile(q, m_tiles, tnt, tmt);
               const int m = tmt * kMp + idx % kMp;
               if (m < p.M) {
-                va[e] = __ldg(p.a_scale + (int64_t)tkb * p.M + m);
-                vb[e] = __ldg(p.b_scale + (int64_t)tnt * KB + tkb);
+                if (p.scalar_scale) {
+                  va[e] = p.a_scale ? __ldg(p.a_scale) : 1.0f;
+                  vb[e] = p.b_scale ? __ldg(p.b_scale) : 1.0f;
+                } else {
+                  va[e] = __ldg(p.a_scale + (int64_t)tkb * p.M + m);
+                  vb[e] = __ldg(p.b_scale + (int64_t)tnt * KB + tkb);
+                }
               }
             }
           }

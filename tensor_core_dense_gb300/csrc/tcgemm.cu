@@ -319,9 +319,11 @@ tcg_status launch_tn_inst(const CUtensorMap& ma, const CUtensorMap& mb, const Ge
 }
 
 // Kernel choice for the dense path: the CTA-pair kernel for problems with at
-// least one full 256 x 256 tile, else the one-SM kernel; for block-scaled FP8,
-// the pair kernel for M > 128, else the skinny one.  TCG_KERNEL=1cta, 2cta or
-// skinny in the environment forces one of them (for tests and measurements).
+// least one full 256 x 256 tile; for M <= 128 the swap-AB skinny kernel where
+// skinny_pays says so; else the one-SM kernel.  For block-scaled FP8: the pair
+// kernel for M > 128 (see gemm_fp8), else the skinny one.  TCG_KERNEL=1cta,
+// 2cta or skinny in the environment forces one of them (for tests and
+// measurements).
 int forced_kernel() {
   const char* e = std::getenv("TCG_KERNEL");
   if (!e) return 0;
@@ -445,6 +447,31 @@ tcg_status launch_block_pair(const Common& a, const float* a_scale, const float*
                : launch_block_pair_inst<1, false>(ma, mb, p, grid, dev, stream);
 }
 
+template <int kIn>
+tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, bool scalar,
+                         cudaStream_t stream);
+
+// Decode-sized problems (M <= 128) are streams of B: the swap-AB skinny
+// kernel spreads them over the SMs in K, where the 128 x 256 tile kernel has
+// only ceil(N/256) tiles.  The rule follows measurements on GB300 (BF16 and
+// FP8, M = 1..128, N = 1024..28672, K = 2048..8192):
+//   M = 1 (a matrix-vector product): always (N = 28672: 81 us against 114);
+//   more N tiles than half the SMs: the 128 x 256 kernel (N = 12288, M = 128:
+//     48 us against 79);
+//   tiles split in two, a CTA pair per tile: always (N = 8192, M = 16: 26.5 us
+//     against 40.4);
+//   tiles split in three: M <= 32, or M <= 64 with at least 64 K steps per
+//     tile (N = 2048, K = 2048, M = 64: 11.6 us against 13.3 lost).
+bool skinny_pays(const Common& a, int in_bytes, int sms) {
+  const int64_t n_tiles = (a.N + 127) / 128;
+  const int64_t steps = (a.K * in_bytes + 127) / 128;
+  if (a.M == 1) return true;
+  if (n_tiles * 2 > sms) return false;
+  if (n_tiles * 3 > sms) return true;
+  if (a.M <= 32) return true;
+  return a.M <= 64 && steps >= 64;
+}
+
 // The persistent 128 x 256 tile kernel (BF16, or per-tensor FP8).
 template <int kIn>
 tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale,
@@ -454,6 +481,8 @@ tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale
   const int fk = forced_kernel();
   if (fk == 2 || (fk == 0 && a.M >= 256 && a.N >= 256))
     return launch_tn2<kIn>(a, a_scale, b_scale, stream, dev, sms);
+  if (a.M <= 128 && (fk == 3 || (fk == 0 && skinny_pays(a, kIn == 0 ? 2 : 1, sms))))
+    return launch_skinny<kIn>(a, a_scale, b_scale, true, stream);
   const int in_bytes = kIn == 0 ? 2 : 1;
   const CUtensorMapDataType dt =
       kIn == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -512,15 +541,21 @@ tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale
                : launch_tn_inst<kIn, 1, false>(ma, mb, p, grid, dev, stream);
 }
 
-template <int kMp>
-tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
+// kIn: 1 = FP8 (block scales, or one scale per tensor when `scalar`), 0 =
+// BF16 (M <= 128, no scales).
+template <int kMp, int kIn>
+tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb, bool scalar,
                               cudaStream_t stream, int dev, int sms) {
   using Cfg = SkinnyCfg<kMp>;
+  if (kIn == 0 && a.M > kMp) return TCG_ERR_UNSUPPORTED;  // BF16: one chunk of A only
+  constexpr int in_bytes = kIn == 1 ? 1 : 2;
+  const CUtensorMapDataType dt =
+      kIn == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap ma, mb;
-  if (tcg_status s = tensor_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.lda, 128, kMp);
+  if (tcg_status s = tensor_map(&ma, dt, a.A, a.K, a.M, a.lda * in_bytes, 128 / in_bytes, kMp);
       s != TCG_OK)
     return s;
-  if (tcg_status s = tensor_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.ldb, 128, 128);
+  if (tcg_status s = tensor_map(&mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, 128 / in_bytes, 128);
       s != TCG_OK)
     return s;
   SkinnyParams p{};
@@ -529,7 +564,8 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   p.K = (int32_t)a.K;
   p.n_tiles = (int32_t)((a.N + 127) / 128);
   p.m_tiles = (int32_t)((a.M + kMp - 1) / kMp);  // 1 unless M > 128 (kMp = 128)
-  p.num_kb = (int32_t)((a.K + 127) / 128);
+  p.num_kb = (int32_t)((a.K * in_bytes + 127) / 128);  // 128-byte steps of K
+  p.scalar_scale = scalar ? 1 : 0;
   const int64_t tiles = (int64_t)p.n_tiles * p.m_tiles;
   const int64_t T = tiles * p.num_kb;
   if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
@@ -568,8 +604,8 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   if (split == 2) {
     // two halves per tile: a cluster of the two CTAs joins them in shared
     // memory (no workspace)
-    auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, true, kMp == 128>
-                             : &gemm_fp8_block_skinny_kernel<kMp, true, false>;
+    auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, true, kMp == 128 && kIn == 1, kIn>
+                             : &gemm_fp8_block_skinny_kernel<kMp, true, false, kIn>;
     if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
     if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 2, ma, mb, p) !=
         cudaSuccess)
@@ -590,8 +626,8 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
         s != TCG_OK)
       return s;
   }
-  auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, false, kMp == 128>
-                           : &gemm_fp8_block_skinny_kernel<kMp, false, false>;
+  auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, false, kMp == 128 && kIn == 1, kIn>
+                           : &gemm_fp8_block_skinny_kernel<kMp, false, false, kIn>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
   if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 1, ma, mb, p) !=
       cudaSuccess)
@@ -600,13 +636,15 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
 
-tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, cudaStream_t stream) {
+template <int kIn>
+tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, bool scalar,
+                         cudaStream_t stream) {
   int dev, sms;
   if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
-  if (a.M <= 16) return launch_skinny_inst<16>(a, sa, sb, stream, dev, sms);
-  if (a.M <= 32) return launch_skinny_inst<32>(a, sa, sb, stream, dev, sms);
-  if (a.M <= 64) return launch_skinny_inst<64>(a, sa, sb, stream, dev, sms);
-  return launch_skinny_inst<128>(a, sa, sb, stream, dev, sms);
+  if (a.M <= 16) return launch_skinny_inst<16, kIn>(a, sa, sb, scalar, stream, dev, sms);
+  if (a.M <= 32) return launch_skinny_inst<32, kIn>(a, sa, sb, scalar, stream, dev, sms);
+  if (a.M <= 64) return launch_skinny_inst<64, kIn>(a, sa, sb, scalar, stream, dev, sms);
+  return launch_skinny_inst<128, kIn>(a, sa, sb, scalar, stream, dev, sms);
 }
 
 // ------------------------------------------------------------ quantiser
@@ -727,7 +765,7 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
     return launch_block_pair(a, a_scale, b_scale, st, dev, sms);
   }
-  return launch_skinny(a, a_scale, b_scale, st);
+  return launch_skinny<1>(a, a_scale, b_scale, false, st);
 }
 
 tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,

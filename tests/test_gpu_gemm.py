@@ -135,6 +135,31 @@ def test_dense_kernels_both_paths(monkeypatch, kernel, M, N, K, kind, out, beta)
     check_full(w, run(w))
 
 
+# M <= 128 BF16 and per-tensor FP8 on the swap-AB skinny kernel (the library
+# routes decode-sized shapes there; TCG_KERNEL=skinny forces it): ragged M,
+# N and K, the cluster-pair split, the general split with the workspace,
+# beta*C, both output types.
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (7, 13, 50), (16, 1000, 1024), (33, 300, 2000),
+                                   (64, 8192, 1024), (100, 2048, 3000), (128, 256, 64),
+                                   (128, 20000, 512)])
+@pytest.mark.parametrize("kind", ["bf16", "fp8"])
+@pytest.mark.parametrize("out,beta", [("f32", 0.0), ("bf16", 1.0)])
+def test_dense_small_m_on_skinny_kernel(monkeypatch, M, N, K, kind, out, beta):
+    monkeypatch.setenv("TCG_KERNEL", "skinny")
+    if kind == "bf16":
+        w = bf16_case(M, N, K, seed=M + 3 * N + K, out=out, alpha=0.75, beta=beta)
+    else:
+        w = fp8_case(M, N, K, seed=M + 3 * N + K, mode="tensor", out=out, beta=beta)
+    check_full(w, run(w))
+
+
+def test_dense_small_m_skinny_deterministic(monkeypatch):
+    monkeypatch.setenv("TCG_KERNEL", "skinny")
+    w = bf16_case(64, 3000, 8192, seed=8, out="f32")
+    d1, d2 = d_to_host(run(w)), d_to_host(run(w))
+    assert np.array_equal(d1.view(np.uint32), d2.view(np.uint32))
+
+
 def test_tail_schedule_deterministic():
     w = bf16_case(1100, 1300, 4096, seed=4, out="f32")
     d1, d2 = d_to_host(run(w)), d_to_host(run(w))
