@@ -21,12 +21,16 @@
  * work on `stream` and returns without synchronising; D is valid once the
  * stream has reached that point.  The library allocates no memory per call:
  * it keeps a process-wide cache of TMA tensor maps (host memory) and, for the
- * split-K skinny path of gemm_fp8_e4m3, a per-device workspace that is
- * allocated on first use and grown when a larger one is needed (that first
- * call therefore must not be made during stream capture).  Calls on
- * different streams may run concurrently, except that calls sharing that
- * workspace are serialised by the stream order the caller gives them; two
- * concurrent skinny calls on different streams of one device race on it.
+ * split-K skinny path of the block-scaled FP8 GEMM, a per-device workspace
+ * that is allocated on first use and grown when a larger one is needed.  A
+ * call that would grow it while its stream is capturing a CUDA graph returns
+ * TCG_ERR_UNSUPPORTED without enqueuing anything (make one call of that size
+ * before capturing, or use gemm_fp8_e4m3_block_noalloc).  Calls on different
+ * streams may run concurrently, except that block-scaled calls on the
+ * split-K skinny kernel (M <= 128, and larger M where the pair tiles would
+ * leave SMs idle) share that workspace and are serialised only by the stream
+ * order the caller gives them; two such calls running concurrently on one
+ * device race on it.  gemm_bf16 and per-tensor FP8 calls never use it.
  *
  * No exception or abort crosses this boundary: every entry point returns a
  * tcg_status.  Argument errors are detected on the host before anything is

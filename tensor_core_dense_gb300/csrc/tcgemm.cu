@@ -205,6 +205,12 @@ tcg_status get_workspace(int dev, size_t counter_bytes, size_t partial_bytes, cu
   std::lock_guard<std::mutex> lk(g_ws_mu);
   Workspace& w = g_ws[dev];
   if (w.counter_cap < cbytes || w.partial_cap < partial_bytes) {
+    // Growing needs cudaDeviceSynchronize and cudaMalloc, which would break a
+    // CUDA graph being captured: refuse instead (the caller makes one call of
+    // the size before capturing, or uses the allocation-free entry point).
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return TCG_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return TCG_ERR_UNSUPPORTED;
     const size_t ccap = w.counter_cap > cbytes ? w.counter_cap : cbytes;
     const size_t pcap = w.partial_cap > partial_bytes ? w.partial_cap : partial_bytes;
     if (w.ptr) {
@@ -453,23 +459,18 @@ tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, bool
 
 // Decode-sized problems (M <= 128) are streams of B: the swap-AB skinny
 // kernel spreads them over the SMs in K, where the 128 x 256 tile kernel has
-// only ceil(N/256) tiles.  The rule follows measurements on GB300 (BF16 and
-// FP8, M = 1..128, N = 1024..28672, K = 2048..8192):
-//   M = 1 (a matrix-vector product): always (N = 28672: 81 us against 114);
-//   more N tiles than half the SMs: the 128 x 256 kernel (N = 12288, M = 128:
-//     48 us against 79);
-//   tiles split in two, a CTA pair per tile: always (N = 8192, M = 16: 26.5 us
-//     against 40.4);
-//   tiles split in three: M <= 32, or M <= 64 with at least 64 K steps per
-//     tile (N = 2048, K = 2048, M = 64: 11.6 us against 13.3 lost).
+// only ceil(N/256) tiles.  It is taken when every N tile splits into exactly
+// two halves joined by a CTA pair in shared memory (N tiles * 2 <= SMs <
+// N tiles * 3, at least two K steps): that form uses no workspace, so these
+// calls keep the dense entry points' properties (no allocation, calls on
+// concurrent streams independent).  Measured on GB300 at N = K = 8192: BF16
+// M = 16 26.1 us against 40.4, per-tensor FP8 15.4 against 21.3.  (Its other
+// splits also won for M <= 32 at smaller N, e.g. BF16 N = 2048, M = 16: 14.2
+// us against 20.1, but they go through the shared split-K workspace.)
 bool skinny_pays(const Common& a, int in_bytes, int sms) {
   const int64_t n_tiles = (a.N + 127) / 128;
   const int64_t steps = (a.K * in_bytes + 127) / 128;
-  if (a.M == 1) return true;
-  if (n_tiles * 2 > sms) return false;
-  if (n_tiles * 3 > sms) return true;
-  if (a.M <= 32) return true;
-  return a.M <= 64 && steps >= 64;
+  return n_tiles * 2 <= sms && n_tiles * 3 > sms && steps >= 2;
 }
 
 // The persistent 128 x 256 tile kernel (BF16, or per-tensor FP8).

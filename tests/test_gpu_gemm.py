@@ -579,6 +579,44 @@ def test_d_aliases_c_in_place(monkeypatch, case, out):
     check_full(w, D)
 
 
+def test_workspace_growth_refused_during_graph_capture(monkeypatch):
+    """A block-scaled call on the split-K skinny kernel whose workspace would
+    have to grow while its stream captures a CUDA graph is refused before
+    anything is enqueued (growing synchronises and allocates, which would
+    break the capture); the capture stays usable and the same call succeeds
+    outside it.  65,536 tiles (64 chunks of A x 1,024 N tiles) need more
+    tile counters than any other test."""
+    import tensor_core_dense_gb300 as tcg
+    monkeypatch.setenv("TCG_KERNEL", "skinny")
+    M, N, K = 8192, 131072, 256  # two K steps: tiles split over CTAs, partials in the workspace
+    A = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    B = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    sa = torch.ones(M * (K // 128), device="cuda")
+    sb = torch.ones((N // 128) * (K // 128), device="cuda")
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    probe = torch.zeros(4, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        probe.add_(1.0)
+        st = tcg.gemm_fp8_e4m3_raw(M, N, K, A.data_ptr(), K, B.data_ptr(), K, sa.data_ptr(),
+                                   sb.data_ptr(), tcg.SCALE_BLOCK128, None, 0, D.data_ptr(), N,
+                                   tcg.OUT_BF16, 1.0, 0.0, side.cuda_stream)
+    assert st == tcg.ERR_UNSUPPORTED
+    g.replay()
+    torch.cuda.synchronize()
+    assert probe.tolist() == [1.0] * 4
+    st = tcg.gemm_fp8_e4m3_raw(M, N, K, A.data_ptr(), K, B.data_ptr(), K, sa.data_ptr(),
+                               sb.data_ptr(), tcg.SCALE_BLOCK128, None, 0, D.data_ptr(), N,
+                               tcg.OUT_BF16, 1.0, 0.0, torch.cuda.current_stream().cuda_stream)
+    assert st == tcg.OK
+    torch.cuda.synchronize()
+    assert (D[::1024, ::4096].float() == 0).all()
+    del D
+    torch.cuda.empty_cache()
+
+
 def test_fp8_block_pair_output_beyond_2_31_elements():
     """Block-scaled FP8 on the pair-tile kernel with a 65,600 x 32,768 output
     (2.15e9 elements, 4.3 GB of BF16) and a ragged last tile row: output and
