@@ -31,13 +31,13 @@
 // writes D.  Only the first and the last piece of a CTA's range can be
 // partial tiles.
 //
-// When every tile is split into exactly two halves (kPair: N tiles * 2 <=
-// SMs < N tiles * 3, e.g. N = 8192), the two CTAs of a tile form a cluster
-// instead: each leaves its FP32 partial in its own shared memory, and after a
-// cluster barrier CTA r adds the two halves (lower K range first, so the
-// result is the same every run) for half of the tile's outputs, reading the
-// peer's partial over distributed shared memory -- no workspace, no atomics,
-// no global round trip at the end.
+// When every tile is split into exactly kJoin = 2 or 3 pieces (N tiles *
+// kJoin <= SMs, e.g. N = 8192 in two, N <= 6400 in three), the CTAs of a tile
+// form a cluster instead: each leaves its FP32 partial in its own shared
+// memory, and after a cluster barrier CTA r adds the pieces (lowest K range
+// first, so the result is the same every run) for its share of the tile's
+// outputs, reading the others' partials over distributed shared memory -- no
+// workspace, no atomics, no global round trip at the end.
 //
 // Roles: warp 0 TMA producer (one lane), warp 1 TMEM allocator + MMA issuer
 // (one lane), then two (Mp <= 32) or four (Mp >= 64) epilogue warpgroups;
@@ -182,7 +182,10 @@ __device__ __forceinline__ void emit_four(const SkinnyParams& p, int m, int n, f
 // constant 1, so the chunk index folds away (M <= 128 keeps its lean code).
 // kIn: 1 = FP8 (kind::f8f6f4, 128 K elements per step), 0 = BF16 (kind::f16,
 // 64 K elements per step: a step is 128 bytes of K either way).
-template <int kMp, bool kPair, bool kMChunks, int kIn = 1>
+// kJoin: 0 = partial tiles through the global workspace; 2 or 3 = every tile
+// is split into kJoin pieces computed by the CTAs of one cluster, which join
+// them in distributed shared memory.
+template <int kMp, int kJoin, bool kMChunks, int kIn = 1>
 __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     gemm_fp8_block_skinny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                  const __grid_constant__ CUtensorMap tmap_b,
@@ -442,8 +445,8 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
       // ---- this CTA's K range of tile nt is summed
       const int64_t tile_first = st - kb;
       const int kb_first = (int)((tile_first > s0 ? tile_first : s0) - tile_first);
-      if (kPair) {
-        // park the half-tile partial in this CTA's shared memory (every MMA
+      if (kJoin > 0) {
+        // park this piece's partial in this CTA's shared memory (every MMA
         // and TMA copy of the range is complete: the stages are free)
         float* part = reinterpret_cast<float*>(gbase);
 #pragma unroll
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     }
     // ---- end of the range: count this CTA's partial tiles in, and finish
     // the tiles it is the last contributor to.
-    if (!kPair && ok && npend > 0) {
+    if (kJoin == 0 && ok && npend > 0) {
       __threadfence();
       __syncwarp();
       if (lane == 0) mbar_arrive(seg_bar);
@@ -546,28 +549,34 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  if (kPair) {
-    cluster_sync_all();  // both halves' partials are in shared memory
+  if constexpr (kJoin > 0) {
+    cluster_sync_all();  // every piece's partial is in shared memory
     if (warp >= 2 && !*abort_flag) {
-      // CTA r finishes float4 units [r*kUnits/2, (r+1)*kUnits/2) of the
-      // Mp x 128 tile (a unit is 4 consecutive n of one row m)
+      // CTA r finishes float4 units [r*kPer, (r+1)*kPer) of the Mp x 128 tile
+      // (a unit is 4 consecutive n of one row m), adding the pieces in
+      // cluster-rank order, which is K order: the same result every run
       constexpr int kUnits = kMp * 32;
+      constexpr int kPer = (kUnits + kJoin - 1) / kJoin;
       const uint32_t rank = cluster_ctarank();
       const uint32_t local = smem_u32(gbase);
-      const uint32_t lo_half = map_shared_to_cta(local, 0);  // K blocks [0, KB/2)
-      const uint32_t hi_half = map_shared_to_cta(local, 1);
+      uint32_t piece[kJoin];
+#pragma unroll
+      for (int r = 0; r < kJoin; ++r) piece[r] = map_shared_to_cta(local, (uint32_t)r);
       int tnt, tmt;
       sk_tile((int)s0 / KB, m_tiles, tnt, tmt);
       const int etid = (int)((warp - 2) * 32u + lane);
-      for (int u = (int)rank * (kUnits / 2) + etid; u < ((int)rank + 1) * (kUnits / 2);
-           u += kSkEpiThreads) {
-        const float4 a = ld_shared_cluster_v4(lo_half + 16u * (uint32_t)u);
-        const float4 b = ld_shared_cluster_v4(hi_half + 16u * (uint32_t)u);
-        emit_four(p, tmt * kMp + (u >> 5), tnt * 128 + (u & 31) * 4,
-                  make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+      const int u_end = ((int)rank + 1) * kPer < kUnits ? ((int)rank + 1) * kPer : kUnits;
+      for (int u = (int)rank * kPer + etid; u < u_end; u += kSkEpiThreads) {
+        float4 sum = ld_shared_cluster_v4(piece[0] + 16u * (uint32_t)u);
+#pragma unroll
+        for (int r = 1; r < kJoin; ++r) {
+          const float4 v = ld_shared_cluster_v4(piece[r] + 16u * (uint32_t)u);
+          sum = make_float4(sum.x + v.x, sum.y + v.y, sum.z + v.z, sum.w + v.w);
+        }
+        emit_four(p, tmt * kMp + (u >> 5), tnt * 128 + (u & 31) * 4, sum);
       }
     }
-    cluster_sync_all();  // the peer has finished reading this CTA's partial
+    cluster_sync_all();  // the other CTAs have finished reading this CTA's partial
   }
   if (warp == 1) {
     __syncwarp();

@@ -459,18 +459,18 @@ tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, bool
 
 // Decode-sized problems (M <= 128) are streams of B: the swap-AB skinny
 // kernel spreads them over the SMs in K, where the 128 x 256 tile kernel has
-// only ceil(N/256) tiles.  It is taken when every N tile splits into exactly
-// two halves joined by a CTA pair in shared memory (N tiles * 2 <= SMs <
-// N tiles * 3, at least two K steps): that form uses no workspace, so these
-// calls keep the dense entry points' properties (no allocation, calls on
-// concurrent streams independent).  Measured on GB300 at N = K = 8192: BF16
-// M = 16 26.1 us against 40.4, per-tensor FP8 15.4 against 21.3.  (Its other
-// splits also won for M <= 32 at smaller N, e.g. BF16 N = 2048, M = 16: 14.2
-// us against 20.1, but they go through the shared split-K workspace.)
+// only ceil(N/256) tiles.  It is taken when every N tile splits into two or
+// three pieces joined by a cluster in shared memory (N tiles * 2 <= SMs, at
+// least two K steps): that form uses no workspace, so these calls keep the
+// dense entry points' properties (no allocation, calls on concurrent streams
+// independent).  Measured on GB300: BF16 M = 16, N = K = 8192 (pairs): 26.1
+// us against 40.4; N = 2048, K = 4096 (clusters of three): 11.0 against 20.2;
+// M = 128, N = 4096, K = 4096: 15.8 against 21.3; per-tensor FP8 M = 64,
+// N = 2048, K = 2048: 6.8 against 7.2.
 bool skinny_pays(const Common& a, int in_bytes, int sms) {
   const int64_t n_tiles = (a.N + 127) / 128;
   const int64_t steps = (a.K * in_bytes + 127) / 128;
-  return n_tiles * 2 <= sms && n_tiles * 3 > sms && steps >= 2;
+  return n_tiles * 2 <= sms && steps >= 2;
 }
 
 // The persistent 128 x 256 tile kernel (BF16, or per-tensor FP8).
@@ -542,6 +542,56 @@ tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale
                : launch_tn_inst<kIn, 1, false>(ma, mb, p, grid, dev, stream);
 }
 
+// The skinny kernel with its tiles split over clusters of kJoin CTAs.
+template <int kMp, int kJoin, int kIn>
+tcg_status launch_skinny_join(bool chunks, const CUtensorMap& ma, const CUtensorMap& mb,
+                              const SkinnyParams& p, cudaStream_t stream, int dev) {
+  using Cfg = SkinnyCfg<kMp>;
+  auto* fn = chunks ? &gemm_fp8_block_skinny_kernel<kMp, kJoin, kMp == 128 && kIn == 1, kIn>
+                    : &gemm_fp8_block_skinny_kernel<kMp, kJoin, false, kIn>;
+  if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
+  if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, kJoin, ma, mb, p) !=
+      cudaSuccess)
+    return TCG_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+// Whether `tiles` clusters of three skinny CTAs can be resident at once (a
+// cluster must fit in one GPC, so fewer than SMs/3 may fit); asked once per
+// kernel and device.
+template <int kMp, int kIn>
+bool skinny_trio_fits(bool chunks, int64_t tiles, int dev) {
+  using Cfg = SkinnyCfg<kMp>;
+  static int max_clusters[2][kMaxDevices] = {};
+  auto* fn = chunks ? &gemm_fp8_block_skinny_kernel<kMp, 3, kMp == 128 && kIn == 1, kIn>
+                    : &gemm_fp8_block_skinny_kernel<kMp, 3, false, kIn>;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  int& n = max_clusters[chunks ? 1 : 0][dev];
+  if (n == 0) {
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Cfg::kSmemBytes) != cudaSuccess)
+      return false;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(3, 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 3;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
+      n = -1;  // unknown: use pairs
+      cudaGetLastError();
+    }
+  }
+  return n > 0 && tiles <= n;
+}
+
 // kIn: 1 = FP8 (block scales, or one scale per tensor when `scalar`), 0 =
 // BF16 (M <= 128, no scales).
 template <int kMp, int kIn>
@@ -602,17 +652,16 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   p.beta = a.beta;
   p.out_f32 = a.out == TCG_OUT_F32;
   p.has_c = a.beta != 0.0f;
-  if (split == 2) {
-    // two halves per tile: a cluster of the two CTAs joins them in shared
-    // memory (no workspace)
-    auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, true, kMp == 128 && kIn == 1, kIn>
-                             : &gemm_fp8_block_skinny_kernel<kMp, true, false, kIn>;
-    if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
-    if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 2, ma, mb, p) !=
-        cudaSuccess)
-      return TCG_ERR_CUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+  if (split == 3 && !skinny_trio_fits<kMp, kIn>(p.m_tiles > 1, tiles, dev)) {
+    split = 2;  // fewer clusters of three fit at once than there are tiles
+    p.grid = (int32_t)(tiles * 2);
+  }
+  if (split == 2 || split == 3) {
+    // two or three pieces per tile: a cluster of their CTAs joins them in
+    // shared memory (no workspace)
+    if (split == 2)
+      return launch_skinny_join<kMp, 2, kIn>(p.m_tiles > 1, ma, mb, p, stream, dev);
+    return launch_skinny_join<kMp, 3, kIn>(p.m_tiles > 1, ma, mb, p, stream, dev);
   }
   // Segments per tile: a tile of num_kb steps meets at most
   // ceil(num_kb / min_range) + 1 ranges, min_range = floor(T / grid).
@@ -627,8 +676,8 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
         s != TCG_OK)
       return s;
   }
-  auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, false, kMp == 128 && kIn == 1, kIn>
-                           : &gemm_fp8_block_skinny_kernel<kMp, false, false, kIn>;
+  auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, 0, kMp == 128 && kIn == 1, kIn>
+                           : &gemm_fp8_block_skinny_kernel<kMp, 0, false, kIn>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
   if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 1, ma, mb, p) !=
       cudaSuccess)
@@ -970,7 +1019,7 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
   p.beta = a.beta;
   p.out_f32 = a.out == TCG_OUT_F32;
   p.has_c = a.beta != 0.0f;
-  auto* fn = &gemm_fp8_block_skinny_kernel<kMp, false, false>;  // M <= 128: one chunk
+  auto* fn = &gemm_fp8_block_skinny_kernel<kMp, 0, false>;  // M <= 128: one chunk
   {  // raise the shared-memory limit once per device (no host-side table)
     static bool raised[kMaxDevices] = {};
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
