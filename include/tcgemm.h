@@ -147,7 +147,9 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
  *
  * Arguments, layouts, alignment and numerics are those of gemm_fp8_e4m3 with
  * mode = TCG_SCALE_BLOCK128.  M > 128 runs on the CTA-pair kernel, which
- * needs no scratch.  For M <= 128 the split-K scratch is a fixed 32 MiB array
+ * needs no scratch; so does M <= 128 when every N tile splits into two or
+ * three pieces joined by a cluster (ceil(N/128) * 2 <= SMs).  Otherwise, for
+ * M <= 128, the split-K scratch is a fixed 32 MiB array
  * inside the library's device code, present on every device that loads the
  * library until the process exits; the caller still provides A, B, the
  * scales, C and D.  A problem whose scratch would exceed 32 MiB (counters:

@@ -960,6 +960,31 @@ tcg_status encode_map_uncached(CUtensorMap* out, const void* ptr, uint64_t inner
              : TCG_ERR_CUDA;
 }
 
+// The cluster-join forms of the skinny kernel without the host-side table
+// (a per-device flag raises the shared-memory limit).
+template <int kMp, int kJoin>
+tcg_status launch_skinny_join_noalloc(const CUtensorMap& ma, const CUtensorMap& mb,
+                                      const SkinnyParams& p, cudaStream_t stream, int dev) {
+  using Cfg = SkinnyCfg<kMp>;
+  auto* fn = &gemm_fp8_block_skinny_kernel<kMp, kJoin, false>;
+  {
+    static bool raised[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!raised[dev]) {
+      if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Cfg::kSmemBytes) != cudaSuccess)
+        return TCG_ERR_CUDA;
+      raised[dev] = true;
+    }
+  }
+  if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, kJoin, ma, mb, p) !=
+      cudaSuccess)
+    return TCG_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
 template <int kMp>
 tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* sb,
                                  cudaStream_t stream, int dev, int sms) {
@@ -979,10 +1004,11 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
   // few partial sums to add; otherwise the steps are spread over all SMs and
   // every CTA gets at least ceil(KB/3) of them.  Either way at most kSkMaxSeg
   // (4) CTAs share a tile.
+  int64_t split = 0;
   {
     int64_t g;
     if (p.n_tiles < sms) {
-      int64_t split = sms / p.n_tiles;
+      split = sms / p.n_tiles;
       if (split > 3) split = 3;
       if (split > p.num_kb) split = p.num_kb;
       g = p.n_tiles * split;
@@ -992,6 +1018,27 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
       if (g > sms) g = sms;
     }
     p.grid = (int32_t)(g < 1 ? 1 : g);
+  }
+  if (split == 3 && !skinny_trio_fits<kMp, 1>(false, p.n_tiles, dev)) {
+    split = 2;
+    p.grid = (int32_t)(p.n_tiles * 2);
+  }
+  if (split == 2 || split == 3) {  // cluster join: no scratch at all
+    CUtensorMap ma, mb;
+    if (tcg_status s = encode_map_uncached(&ma, a.A, a.K, a.M, a.lda, kMp); s != TCG_OK) return s;
+    if (tcg_status s = encode_map_uncached(&mb, a.B, a.K, a.N, a.ldb, 128); s != TCG_OK) return s;
+    p.a_scale = sa;
+    p.b_scale = sb;
+    p.C = a.beta != 0.0f ? a.C : nullptr;
+    p.ldc = a.ldc;
+    p.D = a.D;
+    p.ldd = a.ldd;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.out_f32 = a.out == TCG_OUT_F32;
+    p.has_c = a.beta != 0.0f;
+    return split == 2 ? launch_skinny_join_noalloc<kMp, 2>(ma, mb, p, stream, dev)
+                      : launch_skinny_join_noalloc<kMp, 3>(ma, mb, p, stream, dev);
   }
   const int64_t min_range = T / p.grid;
   p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);

@@ -44,13 +44,16 @@ def _case(M, N, K, seed, out, beta):
     return w
 
 
-# M <= 128 runs the skinny kernel with the fixed scratch; M > 128 the
-# pair-tile kernel, which needs none (the regular entry point may pick the
-# chunked skinny kernel for the same shape: 300 x 1000).
+# M <= 128 runs the skinny kernel: its cluster joins (tiles in three: 4096,
+# 2048 columns; in two: 8192) need no scratch, more N tiles than SMs (20000
+# columns) use the fixed scratch; M > 128 the pair-tile kernel, which needs
+# none (the regular entry point may pick the chunked skinny kernel for the
+# same shape: 300 x 1000).
 @pytest.mark.parametrize("M,N,K,out,beta", [(64, 4096, 4096, "f32", 0.0),
                                             (16, 8192, 8192, "bf16", 0.0),
                                             (100, 2048, 3000, "bf16", -1.0),
                                             (128, 8192, 8192, "f32", 0.0),
+                                            (32, 20000, 1024, "f32", 1.0),
                                             (300, 1000, 1024, "bf16", 1.0),
                                             (1024, 2048, 2048, "f32", 0.0)])
 def test_noalloc_matches_regular_entry_point_twice(M, N, K, out, beta):
