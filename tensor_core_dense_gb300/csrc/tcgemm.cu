@@ -489,12 +489,15 @@ tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale
       kIn == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint32_t box_k = kBKBytes / in_bytes;
   CUtensorMap ma, mb;
-  if (tcg_status s = tensor_map(&ma, dt, a.A, a.K, a.M, a.lda * in_bytes, box_k, kBM); s != TCG_OK)
+  const uint32_t a_rows = a.M < kBM ? (uint32_t)((a.M + 7) / 8 * 8) : (uint32_t)kBM;
+  if (tcg_status s = tensor_map(&ma, dt, a.A, a.K, a.M, a.lda * in_bytes, box_k, a_rows);
+      s != TCG_OK)
     return s;
   if (tcg_status s = tensor_map(&mb, dt, a.B, a.K, a.N, a.ldb * in_bytes, box_k, kBBoxRows);
       s != TCG_OK)
     return s;
   GemmParams p{};
+  p.a_rows = a_rows;
   p.M = (int32_t)a.M;
   p.N = (int32_t)a.N;
   p.K = (int32_t)a.K;

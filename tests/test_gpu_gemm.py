@@ -125,7 +125,8 @@ def test_tail_schedules(M, N, K, kind, out, beta):
     (1, 8, 8, "bf16", "f32", 0.0), (129, 257, 65, "bf16", "bf16", 1.0),
     (1000, 1000, 2048, "fp8", "bf16", 0.0), (2048, 2560, 1024, "bf16", "f32", -0.5),
     (4096, 2560, 512, "fp8", "f32", 0.0), (777, 3000, 1111, "bf16", "bf16", 1.0),
-    (2048, 4096, 512, "bf16", "f32", 0.0)])
+    (2048, 4096, 512, "bf16", "f32", 0.0), (3, 3000, 1000, "fp8", "bf16", 1.0),
+    (5, 1000, 4100, "bf16", "f32", 0.0), (12, 700, 2000, "fp8", "f32", 0.0)])
 def test_dense_kernels_both_paths(monkeypatch, kernel, M, N, K, kind, out, beta):
     monkeypatch.setenv("TCG_KERNEL", kernel)
     if kind == "bf16":
