@@ -100,9 +100,7 @@ struct SkinnyParams {
   float alpha, beta;
   int32_t out_f32, has_c;
   uint32_t fp8_fmt;  // UMMA A (= B, the weights) / UMMA B (= A) format fields
-  // 1: one scale for the whole problem, a_scale[0] * b_scale[0] (per-tensor
-  // FP8; 1 when a pointer is null, as for BF16) instead of the block tables
-  int32_t scalar_scale;
+  int32_t pad_;
   float* ws;               // [grid][2][Mp][128] partial sums: a CTA's first and last piece
   unsigned int* counters;  // [n_tiles * m_tiles], zero between calls
 };
@@ -185,13 +183,21 @@ __device__ __forceinline__ void emit_four(const SkinnyParams& p, int m, int n, f
 // kJoin: 0 = partial tiles through the global workspace; 2 or 3 = every tile
 // is split into kJoin pieces computed by the CTAs of one cluster, which join
 // them in distributed shared memory.
-template <int kMp, int kJoin, bool kMChunks, int kIn = 1>
+// kScalar: one scale for the whole problem, a_scale[0] * b_scale[0] (per-
+// tensor FP8; 1 for a null pointer, as for BF16): no scale table.  With Mp =
+// 128, where nothing changes across K, the MMA also accumulates a CTA's whole
+// piece of a tile in Tensor Memory and the epilogue drains it once instead of
+// promoting every step (N = K = 8192: BF16 36.3 -> 34.2 us); for smaller Mp
+// the MMAs into one accumulator serialise (BF16 M = 16: 26.1 -> 29.5 us), so
+// those keep one buffer per step and promote with the one scale.
+template <int kMp, int kJoin, bool kMChunks, int kIn = 1, bool kScalar = false>
 __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     gemm_fp8_block_skinny_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                  const __grid_constant__ CUtensorMap tmap_b,
                                  const SkinnyParams p) {
   using Cfg = SkinnyCfg<kMp>;
   constexpr int kKElems = kIn == 1 ? 128 : 64;  // K elements per 128-byte step
+  constexpr bool kAccTmem = kScalar && kMp == 128;  // a piece accumulates in TMEM
   constexpr int S = Cfg::kStages;
   constexpr int kHalf = Cfg::kHalf;
   constexpr int kSkNumAcc = Cfg::kNumAcc;
@@ -303,11 +309,16 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     // ------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t j = 0;
+      uint32_t pc = 0;  // kScalar: pieces (a CTA's part of one tile) so far
       bool ok = true, issued = false;
       for (int64_t st = s0; st < s1; ++st, ++j) {
         const uint32_t s = j % S, ph = (j / S) & 1u;
-        const uint32_t b = j % kSkNumAcc, bph = (j / kSkNumAcc) & 1u;
-        if (!wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, 0x12) ||
+        const int kbs = (int)st - ((int)st / KB) * KB;
+        const bool piece_start = !kAccTmem || st == s0 || kbs == 0;
+        const bool piece_end = !kAccTmem || kbs == KB - 1 || st == s1 - 1;
+        const uint32_t slot = kAccTmem ? pc : j;  // TMEM buffer sequence number
+        const uint32_t b = slot % kSkNumAcc, bph = (slot / kSkNumAcc) & 1u;
+        if ((piece_start && !wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, 0x12)) ||
             !wait_phase(full_bar(s), ph, abort_flag, 0x13)) {
           ok = false;
           break;
@@ -318,14 +329,18 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
         const uint32_t d_tmem = tmem_base + b * kMp;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // 32 bytes of K per instruction
+          const uint32_t accumulate = (k != 0 || !piece_start) ? 1u : 0u;
           if (kIn == 1)
-            mma_e4m3(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, k != 0);
+            mma_e4m3(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, accumulate);
           else
-            mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, k != 0);
+            mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, accumulate);
         }
         issued = true;
         tc_commit(empty_bar(s));
-        tc_commit(tfull_bar(b));
+        if (piece_end) {
+          tc_commit(tfull_bar(b));
+          ++pc;
+        }
       }
       if (!ok && issued) {
         tc_commit(drain_bar);
@@ -355,6 +370,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
       return __shfl_sync(0xFFFFFFFFu, okg, 0) != 0;
     };
     uint32_t j = 0;
+    uint32_t pc = 0;  // kScalar: pieces drained so far
     int pend_nt[2];  // partial tiles of this range (its first and last piece)
     int npend = 0;
     bool ok = true;
@@ -362,8 +378,11 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     float acc[kHalf];
 #pragma unroll
     for (int c = 0; c < kHalf; ++c) acc[c] = 0.0f;
+    float s_scalar = 1.0f;  // kScalar: the one scale product
+    if (kScalar)
+      s_scalar = (p.a_scale ? __ldg(p.a_scale) : 1.0f) * (p.b_scale ? __ldg(p.b_scale) : 1.0f);
     for (; ok && st < s1; ++st, ++j) {
-      if (st == tab_end) {
+      if (!kScalar && st == tab_end) {
         // Next chunk of the scale-product table: every load in flight at once.
         if (st != s0 && !group_sync(0x17)) {  // everyone is done with the old chunk
           ok = false;
@@ -388,13 +407,8 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
               sk_tile(q, m_tiles, tnt, tmt);
               const int m = tmt * kMp + idx % kMp;
               if (m < p.M) {
-                if (p.scalar_scale) {
-                  va[e] = p.a_scale ? __ldg(p.a_scale) : 1.0f;
-                  vb[e] = p.b_scale ? __ldg(p.b_scale) : 1.0f;
-                } else {
-                  va[e] = __ldg(p.a_scale + (int64_t)tkb * p.M + m);
-                  vb[e] = __ldg(p.b_scale + (int64_t)tnt * KB + tkb);
-                }
+                va[e] = __ldg(p.a_scale + (int64_t)tkb * p.M + m);
+                vb[e] = __ldg(p.b_scale + (int64_t)tnt * KB + tkb);
               }
             }
           }
@@ -411,7 +425,9 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
       }
       const int nt = (int)st / KB;  // tile index (N tile and M chunk)
       const int kb = (int)st - nt * KB;
-      const uint32_t b = j % kSkNumAcc, bph = (j / kSkNumAcc) & 1u;
+      if (kAccTmem && !(kb == KB - 1 || st == s1 - 1)) continue;  // the MMA keeps accumulating
+      const uint32_t slot = kAccTmem ? pc : j;  // TMEM buffer sequence number
+      const uint32_t b = slot % kSkNumAcc, bph = (slot / kSkNumAcc) & 1u;
       uint32_t got = 0;
       if (lane == 0) got = wait_phase(tfull_bar(b), bph, abort_flag, 0x14) ? 1u : 0u;
       got = __shfl_sync(0xFFFFFFFFu, got, 0);
@@ -420,21 +436,36 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const float* sc = stab + (st - tab_begin) * kMp + col0;
+      const float* sc = kScalar ? stab : stab + (st - tab_begin) * kMp + col0;  // (no table)
       // Drain the partial in pieces of at most 32 columns (register budget).
       constexpr int kPiece = kHalf < 32 ? kHalf : 32;
+      if constexpr (kAccTmem) {
+        // the whole piece's sum, once: acc (zero here) = sum * scale
 #pragma unroll
-      for (int c1 = 0; c1 < kHalf; c1 += kPiece) {
-        uint32_t r[kPiece];
-        tmem_load_cols<kPiece>(
-            tmem_base + ((q * 32u) << 16) + b * kMp + (uint32_t)(col0 + c1), r);
+        for (int c1 = 0; c1 < kHalf; c1 += kPiece) {
+          uint32_t r[kPiece];
+          tmem_load_cols<kPiece>(
+              tmem_base + ((q * 32u) << 16) + b * kMp + (uint32_t)(col0 + c1), r);
 #pragma unroll
-        for (int c = 0; c < kPiece; c += 4) {
-          // acc += partial * scale product, two columns per packed f32x2 FMA
-          // (each lane rounded as fmaf)
-          const float4 s4 = *reinterpret_cast<const float4*>(sc + c1 + c);
-          fma_f32x2_pair(acc[c1 + c + 0], acc[c1 + c + 1], r[c + 0], r[c + 1], s4.x, s4.y);
-          fma_f32x2_pair(acc[c1 + c + 2], acc[c1 + c + 3], r[c + 2], r[c + 3], s4.z, s4.w);
+          for (int c = 0; c < kPiece; ++c)
+            acc[c1 + c] = fmaf(__uint_as_float(r[c]), s_scalar, acc[c1 + c]);
+        }
+        ++pc;
+      } else {
+#pragma unroll
+        for (int c1 = 0; c1 < kHalf; c1 += kPiece) {
+          uint32_t r[kPiece];
+          tmem_load_cols<kPiece>(
+              tmem_base + ((q * 32u) << 16) + b * kMp + (uint32_t)(col0 + c1), r);
+#pragma unroll
+          for (int c = 0; c < kPiece; c += 4) {
+            // acc += partial * scale product, two columns per packed f32x2 FMA
+            // (each lane rounded as fmaf)
+            const float4 s4 = kScalar ? make_float4(s_scalar, s_scalar, s_scalar, s_scalar)
+                                      : *reinterpret_cast<const float4*>(sc + c1 + c);
+            fma_f32x2_pair(acc[c1 + c + 0], acc[c1 + c + 1], r[c + 0], r[c + 1], s4.x, s4.y);
+            fma_f32x2_pair(acc[c1 + c + 2], acc[c1 + c + 3], r[c + 2], r[c + 3], s4.z, s4.w);
+          }
         }
       }
       tc_fence_before_sync();

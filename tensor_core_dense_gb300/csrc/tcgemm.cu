@@ -546,12 +546,13 @@ tcg_status launch_tn(const Common& a, const float* a_scale, const float* b_scale
 }
 
 // The skinny kernel with its tiles split over clusters of kJoin CTAs.
-template <int kMp, int kJoin, int kIn>
+template <int kMp, int kJoin, int kIn, bool kScalar>
 tcg_status launch_skinny_join(bool chunks, const CUtensorMap& ma, const CUtensorMap& mb,
                               const SkinnyParams& p, cudaStream_t stream, int dev) {
   using Cfg = SkinnyCfg<kMp>;
-  auto* fn = chunks ? &gemm_fp8_block_skinny_kernel<kMp, kJoin, kMp == 128 && kIn == 1, kIn>
-                    : &gemm_fp8_block_skinny_kernel<kMp, kJoin, false, kIn>;
+  constexpr bool kChunks = kMp == 128 && kIn == 1 && !kScalar;  // M > 128: block scales only
+  auto* fn = chunks ? &gemm_fp8_block_skinny_kernel<kMp, kJoin, kChunks, kIn, kScalar>
+                    : &gemm_fp8_block_skinny_kernel<kMp, kJoin, false, kIn, kScalar>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
   if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, kJoin, ma, mb, p) !=
       cudaSuccess)
@@ -563,12 +564,13 @@ tcg_status launch_skinny_join(bool chunks, const CUtensorMap& ma, const CUtensor
 // Whether `tiles` clusters of three skinny CTAs can be resident at once (a
 // cluster must fit in one GPC, so fewer than SMs/3 may fit); asked once per
 // kernel and device.
-template <int kMp, int kIn>
+template <int kMp, int kIn, bool kScalar>
 bool skinny_trio_fits(bool chunks, int64_t tiles, int dev) {
   using Cfg = SkinnyCfg<kMp>;
   static int max_clusters[2][kMaxDevices] = {};
-  auto* fn = chunks ? &gemm_fp8_block_skinny_kernel<kMp, 3, kMp == 128 && kIn == 1, kIn>
-                    : &gemm_fp8_block_skinny_kernel<kMp, 3, false, kIn>;
+  constexpr bool kChunks = kMp == 128 && kIn == 1 && !kScalar;
+  auto* fn = chunks ? &gemm_fp8_block_skinny_kernel<kMp, 3, kChunks, kIn, kScalar>
+                    : &gemm_fp8_block_skinny_kernel<kMp, 3, false, kIn, kScalar>;
   std::lock_guard<std::mutex> lk(g_attr_mu);
   int& n = max_clusters[chunks ? 1 : 0][dev];
   if (n == 0) {
@@ -595,13 +597,14 @@ bool skinny_trio_fits(bool chunks, int64_t tiles, int dev) {
   return n > 0 && tiles <= n;
 }
 
-// kIn: 1 = FP8 (block scales, or one scale per tensor when `scalar`), 0 =
-// BF16 (M <= 128, no scales).
-template <int kMp, int kIn>
-tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb, bool scalar,
+// kIn: 1 = FP8 (block scales, or one scale per tensor with kScalar), 0 = BF16
+// (M <= 128, no scales, kScalar).
+template <int kMp, int kIn, bool kScalar>
+tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
                               cudaStream_t stream, int dev, int sms) {
   using Cfg = SkinnyCfg<kMp>;
-  if (kIn == 0 && a.M > kMp) return TCG_ERR_UNSUPPORTED;  // BF16: one chunk of A only
+  constexpr bool kChunks = kMp == 128 && kIn == 1 && !kScalar;
+  if (kScalar && a.M > kMp) return TCG_ERR_UNSUPPORTED;  // one chunk of A only
   constexpr int in_bytes = kIn == 1 ? 1 : 2;
   const CUtensorMapDataType dt =
       kIn == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -619,7 +622,6 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   p.n_tiles = (int32_t)((a.N + 127) / 128);
   p.m_tiles = (int32_t)((a.M + kMp - 1) / kMp);  // 1 unless M > 128 (kMp = 128)
   p.num_kb = (int32_t)((a.K * in_bytes + 127) / 128);  // 128-byte steps of K
-  p.scalar_scale = scalar ? 1 : 0;
   const int64_t tiles = (int64_t)p.n_tiles * p.m_tiles;
   const int64_t T = tiles * p.num_kb;
   if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
@@ -655,7 +657,7 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   p.beta = a.beta;
   p.out_f32 = a.out == TCG_OUT_F32;
   p.has_c = a.beta != 0.0f;
-  if (split == 3 && !skinny_trio_fits<kMp, kIn>(p.m_tiles > 1, tiles, dev)) {
+  if (split == 3 && !skinny_trio_fits<kMp, kIn, kScalar>(p.m_tiles > 1, tiles, dev)) {
     split = 2;  // fewer clusters of three fit at once than there are tiles
     p.grid = (int32_t)(tiles * 2);
   }
@@ -663,8 +665,8 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
     // two or three pieces per tile: a cluster of their CTAs joins them in
     // shared memory (no workspace)
     if (split == 2)
-      return launch_skinny_join<kMp, 2, kIn>(p.m_tiles > 1, ma, mb, p, stream, dev);
-    return launch_skinny_join<kMp, 3, kIn>(p.m_tiles > 1, ma, mb, p, stream, dev);
+      return launch_skinny_join<kMp, 2, kIn, kScalar>(p.m_tiles > 1, ma, mb, p, stream, dev);
+    return launch_skinny_join<kMp, 3, kIn, kScalar>(p.m_tiles > 1, ma, mb, p, stream, dev);
   }
   // Segments per tile: a tile of num_kb steps meets at most
   // ceil(num_kb / min_range) + 1 ranges, min_range = floor(T / grid).
@@ -679,8 +681,8 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
         s != TCG_OK)
       return s;
   }
-  auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, 0, kMp == 128 && kIn == 1, kIn>
-                           : &gemm_fp8_block_skinny_kernel<kMp, 0, false, kIn>;
+  auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, 0, kChunks, kIn, kScalar>
+                           : &gemm_fp8_block_skinny_kernel<kMp, 0, false, kIn, kScalar>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
   if (launch_gemm_kernel(fn, p.grid, Cfg::kThreads, Cfg::kSmemBytes, stream, 1, ma, mb, p) !=
       cudaSuccess)
@@ -689,15 +691,25 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
 }
 
+template <int kIn, bool kScalar>
+tcg_status launch_skinny_mp(const Common& a, const float* sa, const float* sb,
+                            cudaStream_t stream) {
+  int dev, sms;
+  if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+  if (a.M <= 16) return launch_skinny_inst<16, kIn, kScalar>(a, sa, sb, stream, dev, sms);
+  if (a.M <= 32) return launch_skinny_inst<32, kIn, kScalar>(a, sa, sb, stream, dev, sms);
+  if (a.M <= 64) return launch_skinny_inst<64, kIn, kScalar>(a, sa, sb, stream, dev, sms);
+  return launch_skinny_inst<128, kIn, kScalar>(a, sa, sb, stream, dev, sms);
+}
+
+// scalar: one scale for the problem (per-tensor FP8, or BF16).
 template <int kIn>
 tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, bool scalar,
                          cudaStream_t stream) {
-  int dev, sms;
-  if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
-  if (a.M <= 16) return launch_skinny_inst<16, kIn>(a, sa, sb, scalar, stream, dev, sms);
-  if (a.M <= 32) return launch_skinny_inst<32, kIn>(a, sa, sb, scalar, stream, dev, sms);
-  if (a.M <= 64) return launch_skinny_inst<64, kIn>(a, sa, sb, scalar, stream, dev, sms);
-  return launch_skinny_inst<128, kIn>(a, sa, sb, scalar, stream, dev, sms);
+  if constexpr (kIn == 1) {
+    if (!scalar) return launch_skinny_mp<1, false>(a, sa, sb, stream);
+  }
+  return launch_skinny_mp<kIn, true>(a, sa, sb, stream);
 }
 
 // ------------------------------------------------------------ quantiser
@@ -1022,7 +1034,7 @@ tcg_status launch_skinny_noalloc(const Common& a, const float* sa, const float* 
     }
     p.grid = (int32_t)(g < 1 ? 1 : g);
   }
-  if (split == 3 && !skinny_trio_fits<kMp, 1>(false, p.n_tiles, dev)) {
+  if (split == 3 && !skinny_trio_fits<kMp, 1, false>(false, p.n_tiles, dev)) {
     split = 2;
     p.grid = (int32_t)(p.n_tiles * 2);
   }
