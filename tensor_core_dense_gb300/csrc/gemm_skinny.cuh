@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     // ------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t j = 0;
-      uint32_t pc = 0;  // kScalar: pieces (a CTA's part of one tile) so far
+      uint32_t pc = 0;  // kAccTmem: pieces (a CTA's part of one tile) so far
       bool ok = true, issued = false;
       for (int64_t st = s0; st < s1; ++st, ++j) {
         const uint32_t s = j % S, ph = (j / S) & 1u;
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
       return __shfl_sync(0xFFFFFFFFu, okg, 0) != 0;
     };
     uint32_t j = 0;
-    uint32_t pc = 0;  // kScalar: pieces drained so far
+    uint32_t pc = 0;  // kAccTmem: pieces drained so far
     int pend_nt[2];  // partial tiles of this range (its first and last piece)
     int npend = 0;
     bool ok = true;
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
     float acc[kHalf];
 #pragma unroll
     for (int c = 0; c < kHalf; ++c) acc[c] = 0.0f;
-    float s_scalar = 1.0f;  // kScalar: the one scale product
+    float s_scalar = 1.0f;  // kScalar: the one scale product (1 for BF16)
     if (kScalar)
       s_scalar = (p.a_scale ? __ldg(p.a_scale) : 1.0f) * (p.b_scale ? __ldg(p.b_scale) : 1.0f);
     for (; ok && st < s1; ++st, ++j) {
