@@ -360,7 +360,7 @@ def time_graph(rot, steps, warmup, sampler=None):
 
 
 SECONDARY = ("bf16_256", "fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64",
-             "fp8_skinny_128", "fp8_block_4096")
+             "fp8_skinny_128", "fp8_block_4096", "bf16_skinny_16")
 
 # The FP8 quantiser on the operands the FP8 workloads cast: (seed, tensor id,
 # rows, cols, granularity, outlier probability).  The values are the FP32

@@ -64,7 +64,7 @@ class Workload:
 
 
 NAMES = ("bf16_256", "bf16_4096", "fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64",
-         "fp8_skinny_128", "fp8_block_4096")
+         "fp8_skinny_128", "fp8_block_4096", "bf16_skinny_16")
 
 
 def make(name: str, *, M=None, N=None, K=None) -> Workload:
@@ -94,6 +94,13 @@ def make(name: str, *, M=None, N=None, K=None) -> Workload:
         w.A = bf16(4, 1, M, K)
         w.B = bf16(4, 2, N, K, p1=0.02)
         w.C = bf16(4, 3, M, N)
+        return w
+    if name == "bf16_skinny_16":
+        # a decode-sized BF16 GEMM: 16 rows of activations against an 8192^2 weight
+        M, N, K = M or 16, N or 8192, K or 8192
+        w = Workload(name, M, N, K, "bf16", "bf16")
+        w.A = bf16(7, 1, M, K)
+        w.B = bf16(7, 2, N, K, p1=0.02)
         return w
     if name == "fp8_block_4096":
         # the block scaling of the skinny workload on a square 4096^3 problem

@@ -341,7 +341,8 @@ def _sampled(w, out, ntiles=16):
     return worst
 
 
-@pytest.mark.parametrize("name", ["bf16_4096", "fp8_4096", "bf16_mlp"])
+@pytest.mark.parametrize("name", ["bf16_4096", "fp8_4096", "bf16_mlp", "fp8_block_4096",
+                                  "bf16_skinny_16"])
 def test_full_size_sampled(name):
     w = W.make(name)
     _sampled(w, out="f32")   # pre-cast check with the same kernel
