@@ -84,6 +84,10 @@ typedef enum {
  *              stores for C and D).
  * Numerics     products accumulate in FP32 on the tensor cores; alpha and beta
  *              are applied in FP32; BF16 output rounds to nearest even.
+ * Kernels      tile kernels by shape; decode-sized calls (M <= 128, with
+ *              ceil(N/128) * 2 <= SMs) run swap-AB with K split over clusters
+ *              of two or three CTAs whose FP32 partial sums are added in a
+ *              fixed order.  Every path is deterministic and none allocates.
  */
 tcg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                      int64_t ldb, const void* C, int64_t ldc, void* D, int64_t ldd,
@@ -96,8 +100,10 @@ tcg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
  * Layouts and alignment as gemm_bf16 with one byte per element of A and B
  * (lda, ldb multiples of 16).  mode selects the scale granularity above; the
  * scales must be finite.
- * TCG_SCALE_TENSOR   the per-tensor product a_scale[0]*b_scale[0]*alpha is
- *                    applied once, in the epilogue.
+ * TCG_SCALE_TENSOR   the per-tensor product a_scale[0]*b_scale[0] multiplies
+ *                    the FP32 sums once, in the epilogue (on the decode-sized
+ *                    path with M <= 64, every 128-byte K step's partial sum
+ *                    before it is added), then alpha.
  * TCG_SCALE_BLOCK128 every 128-wide K block is accumulated on its own and
  *                    promoted into an FP32 register accumulator with its
  *                    scales sa[i,kb] * sb[j/128,kb] ("promotion": partial sums
