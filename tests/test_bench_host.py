@@ -1,0 +1,70 @@
+"""Host-side pieces of bench.py that need no GPU: the clock summary, the check
+that a stored ncu traffic figure belongs to the current kernel sources, and
+the NVML sampler's failure on a machine without a driver (bench then falls
+back to nvidia-smi)."""
+
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _row(sm, power=500.0, hw="Not Active", hw_thermal="Not Active", sw_thermal="Not Active",
+         sw_power="Not Active"):
+    return dict(sm=sm, max=2070.0, power=power, hw=hw, hw_thermal=hw_thermal,
+                sw_thermal=sw_thermal, sw_power=sw_power)
+
+
+def test_clock_summary_median_and_reasons():
+    rows = [_row(2070.0), _row(1800.0, sw_power="Active"), _row(1900.0)]
+    s = bench.ClockSampler.summary(rows)
+    assert s["sm_mhz"] == 1900.0
+    assert s["sm_max_mhz"] == 2070.0
+    assert s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+    s = bench.ClockSampler.summary([_row(1500.0, hw="Active", hw_thermal="Active")])
+    assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+
+def test_clock_summary_without_samples():
+    s = bench.ClockSampler.summary([])
+    assert s["samples"] == 0 and s["sm_mhz"] is None and s["reasons"] == []
+
+
+def test_stored_traffic_only_for_matching_sources(tmp_path, monkeypatch):
+    csrc = tmp_path / "tensor_core_dense_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "k.cuh").write_text("// kernel v1\n")
+    (csrc / "h.cuh").write_text("// helper\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.kernel_source_sha(["k.cuh", "h.cuh"])
+    (tmp_path / "profiles" / "p.md").write_text(
+        "# profile\n\nsource_files: `k.cuh h.cuh`\n"
+        f"source_sha256: `{sha}`\ntraffic_bytes_per_launch: 12345\n")
+    assert bench.stored_traffic("p.md") == 12345
+    (csrc / "k.cuh").write_text("// kernel v2\n")  # the kernel changed since the capture
+    assert bench.stored_traffic("p.md") is None
+    assert bench.stored_traffic("missing.md") is None
+
+
+def test_committed_profile_is_parsed():
+    """The committed headline summary carries a hash and a traffic figure
+    (whether they still match the sources is what the bench line reports)."""
+    text = open(os.path.join(ROOT, "profiles", "gemm_tn2_bf16_4096.md")).read()
+    assert "source_sha256:" in text and "traffic_bytes_per_launch:" in text
+    t = bench.stored_traffic()
+    assert t is None or t > 0
+
+
+def test_nvml_sampler_fails_cleanly_without_a_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises((OSError, AttributeError)):
+        bench.NvmlSampler("GPU-00000000-0000-0000-0000-000000000000")
