@@ -46,7 +46,7 @@ _lib = None
 
 IN_BF16, IN_E4M3 = 0, 1
 Q_TENSOR, Q_ROW128, Q_BLOCK128 = 0, 1, 2
-SCALE_NONE, SCALE_TENSOR, SCALE_BLOCK128 = 0, 1, 2
+SCALE_NONE, SCALE_TENSOR, SCALE_BLOCK128, SCALE_MX32 = 0, 1, 2, 3
 C_BF16, C_F32 = 0, 1
 FP8_E4M3, FP8_E5M2 = 0, 1
 
@@ -72,6 +72,8 @@ class _Args(ctypes.Structure):
         ("beta", ctypes.c_double),
         ("a_fp8", ctypes.c_int32),
         ("b_fp8", ctypes.c_int32),
+        ("a_sf", ctypes.c_void_p),
+        ("b_sf", ctypes.c_void_p),
     ]
 
 
@@ -101,7 +103,7 @@ def _load():
         for name in ("orc_bf16_decode_array", "orc_bf16_encode_array",
                      "orc_e4m3_decode_array", "orc_e4m3_encode_array",
                      "orc_e5m2_decode_array", "orc_e5m2_encode_array",
-                     "orc_cast_bf16_array"):
+                     "orc_e8m0_decode_array", "orc_cast_bf16_array"):
             getattr(lib, name).argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
             getattr(lib, name).restype = None
         lib.orc_gemm_tiles.argtypes = [ctypes.POINTER(_Args), ctypes.c_int64, ctypes.c_void_p,
@@ -112,6 +114,8 @@ def _load():
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, i64,
                                       ctypes.c_void_p]
         lib.orc_quant_fp8.restype = ctypes.c_int
+        lib.orc_mx_sf_offset.argtypes = [i64, i64, i64]
+        lib.orc_mx_sf_offset.restype = i64
         _lib = lib
     return _lib
 
@@ -157,6 +161,23 @@ def e4m3_encode(x) -> np.ndarray:
     return _elementwise("orc_e4m3_encode_array", x, np.float32, np.uint8)
 
 
+def e8m0_decode(bits) -> np.ndarray:
+    """E8M0 bytes -> float64 values 2^(e - 127) (NaN for 0xFF)."""
+    return _elementwise("orc_e8m0_decode_array", bits, np.uint8, np.float64)
+
+
+def mx_sf_bytes(rows, K) -> int:
+    """Bytes of one operand's MX scales: ceil(rows/128) x ceil(ceil(K/32)/4)
+    tiles of 512 bytes."""
+    return -(-rows // 128) * -(-(-(-K // 32)) // 4) * 512
+
+
+def mx_sf_offset(r, kb, K) -> int:
+    """Byte offset of the scale of row r, 32-wide K block kb (oracle.c's
+    orc_mx_sf_offset, the tiled layout)."""
+    return int(_load().orc_mx_sf_offset(int(r), int(kb), -(-(-(-K // 32)) // 4)))
+
+
 def cast_bf16(v) -> np.ndarray:
     """The BF16 output expected for FP64 values v: v -> FP32 -> BF16 (nearest even)."""
     return _elementwise("orc_cast_bf16_array", v, np.float64, np.uint16)
@@ -171,7 +192,7 @@ def default_threads() -> int:
 
 def gemm(M, N, K, A, lda, B, ldb, *, in_type=IN_BF16, scale_mode=SCALE_NONE,
          a_scale=None, b_scale=None, C=None, ldc=0, c_type=C_F32, alpha=1.0, beta=0.0,
-         tiles=None, nthreads=None, a_fp8=FP8_E4M3, b_fp8=FP8_E4M3):
+         tiles=None, nthreads=None, a_fp8=FP8_E4M3, b_fp8=FP8_E4M3, a_sf=None, b_sf=None):
     """Reference values and error bounds for D = alpha*A*B + beta*C.
 
     A: flat uint16 (BF16) or uint8 (FP8) array, element (i, k) at A[i*lda + k];
@@ -181,6 +202,8 @@ def gemm(M, N, K, A, lda, B, ldb, *, in_type=IN_BF16, scale_mode=SCALE_NONE,
        not read when beta == 0.
     a_scale / b_scale: float32 arrays (scale_mode TENSOR: one value each;
        BLOCK128: a_scale[kb*M + i], b_scale[nb*ceil(K/128) + kb]).
+    a_sf / b_sf: scale_mode MX32: uint8 E8M0 scales per 32-wide K block, in
+       the tiled layout of oracle.c (mx_sf_bytes(M, K) / mx_sf_bytes(N, K)).
     tiles: None for the whole M x N output, else a list of (i0, j0, mi, nj).
 
     Returns (v, bound): FP64 arrays.  For tiles=None each is M x N; otherwise a
@@ -201,7 +224,7 @@ def gemm(M, N, K, A, lda, B, ldb, *, in_type=IN_BF16, scale_mode=SCALE_NONE,
             raise ValueError("C too small")
     elif beta != 0.0:
         raise ValueError("C required when beta != 0")
-    if scale_mode != SCALE_NONE:
+    if scale_mode in (SCALE_TENSOR, SCALE_BLOCK128):
         a_scale = np.ascontiguousarray(a_scale, dtype=np.float32).ravel()
         b_scale = np.ascontiguousarray(b_scale, dtype=np.float32).ravel()
         if scale_mode == SCALE_BLOCK128:
@@ -210,9 +233,17 @@ def gemm(M, N, K, A, lda, B, ldb, *, in_type=IN_BF16, scale_mode=SCALE_NONE,
                 raise ValueError("scale arrays too small")
     else:
         a_scale = b_scale = None
+    if scale_mode == SCALE_MX32:
+        a_scale = b_scale = None
+        a_sf = np.ascontiguousarray(a_sf, dtype=np.uint8).ravel()
+        b_sf = np.ascontiguousarray(b_sf, dtype=np.uint8).ravel()
+        if a_sf.size < mx_sf_bytes(M, K) or b_sf.size < mx_sf_bytes(N, K):
+            raise ValueError("MX scale arrays too small")
+    else:
+        a_sf = b_sf = None
     args = _Args(M, N, K, in_type, scale_mode, _ptr(A), lda, _ptr(B), ldb,
                  _ptr(a_scale), _ptr(b_scale), _ptr(C), ldc, c_type, 0,
-                 float(alpha), float(beta), int(a_fp8), int(b_fp8))
+                 float(alpha), float(beta), int(a_fp8), int(b_fp8), _ptr(a_sf), _ptr(b_sf))
     whole = tiles is None
     if whole:
         tiles = [(0, 0, M, N)]

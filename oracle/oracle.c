@@ -53,6 +53,21 @@
  *     b_scale[nb * KB + kb]        scale of B rows 128nb.., K block kb
  *                                   (128 x 128), KB = ceil(K / 128)
  *
+ * Microscaled FP8 (ORC_SCALE_MX32): the hardware block scaling of "How
+ * Blackwell's Tensor Memory Actually Works", section "Quantization became an
+ * allocation problem": D = C + (A x SFA)(B x SFB) with one scale factor per
+ * group of 32 elements along K, for the MX formats an E8M0 byte, a bare
+ * power-of-two exponent (the Open Compute microscaling specification the
+ * page names).  Reading: E8M0 code e is 2^(e - 127), the microscaling
+ * specification's bias, and 0xFF is NaN.  The products of one 32-wide block
+ * are summed exactly (as above), multiplied by 2^(ea - 127) * 2^(eb - 127)
+ * (exact: a power of two), and the blocks are added in K order.  The storage
+ * of the scale bytes is the library's choice, tiles of 128 rows x 4 K blocks
+ * of 512 bytes each (the order the tensor core's scale-factor copy reads):
+ *     tile (r / 128, kb / 4) at byte offset ((r/128) * KT + kb/4) * 512,
+ *     inside it (r % 32) * 16 + ((r / 32) % 4) * 4 + kb % 4,
+ * with KT = ceil(ceil(K / 32) / 4), for A (r = i) and for B (r = j).
+ *
  * Portable C11, no intrinsics; compiled with -ffp-contract=off so x86 and
  * Arm hosts round identically.
  */
@@ -67,6 +82,7 @@
 #define ORC_SCALE_NONE 0   /* BF16: no scales */
 #define ORC_SCALE_TENSOR 1 /* one scale per operand */
 #define ORC_SCALE_BLOCK128 2
+#define ORC_SCALE_MX32 3   /* E8M0 per 32-wide K block of every row of A and B */
 #define ORC_C_BF16 0
 #define ORC_C_F32 1
 #define ORC_FP8_E4M3 0
@@ -205,6 +221,24 @@ uint8_t orc_e5m2_encode(float f) {
   return (uint8_t)(sign | (uint8_t)(efield << 2) | (uint8_t)(r - 4));
 }
 
+/* E8M0 bits -> value: 2^(e - 127); the code 0xFF is NaN.  No sign, no
+ * mantissa, no zero. */
+double orc_e8m0_decode(uint8_t e) {
+  if (e == 0xFFu) return NAN;
+  return ldexp(1.0, (int)e - 127);
+}
+
+void orc_e8m0_decode_array(const uint8_t* in, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e8m0_decode(in[i]);
+}
+
+/* Byte offset of the scale of row r, 32-wide K block kb in the tiled MX
+ * scale layout (header comment), kt = ceil(ceil(K/32) / 4) tiles along K. */
+int64_t orc_mx_sf_offset(int64_t r, int64_t kb, int64_t kt) {
+  const int64_t tile = (r / 128) * kt + kb / 4;
+  return tile * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + kb % 4;
+}
+
 void orc_e5m2_encode_array(const float* in, int64_t n, uint8_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e5m2_encode(in[i]);
 }
@@ -250,6 +284,8 @@ typedef struct {
   int32_t pad_;
   double alpha, beta;
   int32_t a_fp8, b_fp8; /* FP8 inputs: ORC_FP8_E4M3 / ORC_FP8_E5M2 per operand */
+  const uint8_t* a_sf;  /* ORC_SCALE_MX32: E8M0 scales of A and B, tiled layout */
+  const uint8_t* b_sf;
 } orc_gemm_args;
 
 static double dec_in(const orc_gemm_args* g, const void* base, int64_t idx, int32_t fp8) {
@@ -269,7 +305,22 @@ static void gemm_one(const orc_gemm_args* g, const double* arow, const double* b
                      int64_t j, double* v_out, double* bound_out) {
   const int64_t K = g->K;
   double acc = 0.0, bound = 0.0;
-  if (g->scale_mode == ORC_SCALE_BLOCK128) {
+  if (g->scale_mode == ORC_SCALE_MX32) {
+    const int64_t KB = (K + 31) / 32, KT = (KB + 3) / 4;
+    for (int64_t kb = 0; kb < KB; ++kb) {
+      double part = 0.0, apart = 0.0;
+      int64_t k1 = (kb + 1) * 32 < K ? (kb + 1) * 32 : K;
+      for (int64_t k = kb * 32; k < k1; ++k) {
+        double p = arow[k] * brow[k];
+        part += p;
+        apart += fabs(p);
+      }
+      double s = orc_e8m0_decode(g->a_sf[orc_mx_sf_offset(i, kb, KT)]) *
+                 orc_e8m0_decode(g->b_sf[orc_mx_sf_offset(j, kb, KT)]);
+      acc += part * s;
+      bound += apart * s;
+    }
+  } else if (g->scale_mode == ORC_SCALE_BLOCK128) {
     const int64_t KB = (K + 127) / 128;
     const int64_t nb = j / 128;
     for (int64_t kb = 0; kb < KB; ++kb) {
@@ -368,7 +419,11 @@ int orc_gemm_tiles(const orc_gemm_args* g, int64_t ntiles, const int64_t* tiles,
   if (g->M < 0 || g->N < 0 || g->K < 0) return -1;
   if (g->K > 0 && (!g->A || !g->B)) return -1;
   if (g->beta != 0.0 && !g->C) return -1;
-  if (g->scale_mode != ORC_SCALE_NONE && (!g->a_scale || !g->b_scale)) return -1;
+  if ((g->scale_mode == ORC_SCALE_TENSOR || g->scale_mode == ORC_SCALE_BLOCK128) &&
+      (!g->a_scale || !g->b_scale))
+    return -1;
+  if (g->scale_mode == ORC_SCALE_MX32 && (!g->a_sf || !g->b_sf)) return -1;
+  if (g->scale_mode < ORC_SCALE_NONE || g->scale_mode > ORC_SCALE_MX32) return -1;
   int64_t* offs = (int64_t*)malloc((size_t)(ntiles > 0 ? ntiles : 1) * sizeof(int64_t));
   if (!offs) return -1;
   int64_t o = 0;

@@ -166,3 +166,47 @@ def draw(seed, tensor, ctr) -> int:
     """Raw 64-bit draw `ctr` of stream (seed, tensor)."""
     lib = _load()
     return int(lib.synth_draw(lib.synth_key(seed, tensor), ctr))
+
+
+# ------------------------------------------------------------- microscaling
+
+def mx_tile_sf(exps, K):
+    """E8M0 scale bytes exps[r, kb] (one per row and 32-wide K block) laid out
+    as the library reads them: tiles of 128 rows x 4 K blocks, 512 bytes
+    each, tile (r // 128, kb // 4) at ((r // 128) * KT + kb // 4) * 512 with
+    KT = ceil(ceil(K / 32) / 4); inside a tile, row r % 32 takes 16 bytes,
+    (r // 32) % 4 picks 4 of them and kb % 4 the byte.  Padding rows and
+    blocks hold 127 (scale 1).  Built by reshaping, not by index arithmetic."""
+    exps = np.asarray(exps, dtype=np.uint8)
+    rows = exps.shape[0]
+    KB = -(-K // 32)
+    RT, KT = -(-rows // 128), -(-KB // 4)
+    pad = np.full((RT * 128, KT * 4), 127, dtype=np.uint8)
+    pad[:rows, :KB] = exps[:, :KB]
+    # axes (row tile, (r // 32) % 4, r % 32, K tile, kb % 4) -> tile-major order
+    return np.ascontiguousarray(pad.reshape(RT, 4, 32, KT, 4).transpose(0, 3, 2, 1, 4)).ravel()
+
+
+def mx_quant(x, ld=None, fmt="e4m3"):
+    """Microscaled FP8 of a rows x K float32 matrix: per row and 32-wide K
+    block an E8M0 exponent e and codes FP8(x / 2^(e - 127)), saturating.
+    e = floor(log2(amax)) - emax + 127 with emax = 8 for E4M3 (448 = 1.75 *
+    2^8) and 15 for E5M2, so the block's largest magnitude lands in the
+    format's top binade (the microscaling recipe); an all-zero block takes
+    e = 127.  Returns (q uint8 rows x ld, exps uint8 rows x ceil(K/32))."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, K = x.shape
+    ld = K if ld is None else ld
+    KB = -(-K // 32)
+    xp = np.zeros((rows, KB * 32), np.float32)
+    xp[:, :K] = x
+    amax = np.abs(xp.reshape(rows, KB, 32)).max(axis=2)
+    _, ex = np.frexp(amax)                         # amax = m * 2^ex, 0.5 <= m < 1
+    emax = 8 if fmt == "e4m3" else 15
+    e = np.where(amax > 0, ex - 1 - emax + 127, 127)
+    e = np.clip(e, 0, 254).astype(np.uint8)
+    scaled = np.ldexp(xp.reshape(rows, KB, 32),
+                      -(e.astype(np.int32) - 127)[:, :, None]).reshape(rows, KB * 32)[:, :K]
+    q = np.zeros((rows, ld), np.uint8)
+    q[:, :K] = to_e4m3(scaled) if fmt == "e4m3" else to_e5m2(scaled)
+    return q, e
