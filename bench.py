@@ -326,10 +326,12 @@ class Rotation:
                 f"finds its operands in L2")
 
 
-def time_graph(rot, steps, warmup, sampler=None):
+def time_graph(rot, steps, warmup, sampler=None, replays=1, world=1):
     """Time `steps` back-to-back calls (cycling the copies) replayed from one
-    CUDA graph; returns (total ms, kernel launches inside the graph).  A
-    sampler (start/stop) runs exactly around the timed replay."""
+    CUDA graph, `replays` times; returns (list of ms per replay, kernel
+    launches inside the graph, graph).  Each replay is bracketed by a barrier
+    and a device synchronisation; a sampler (start/stop) runs around the timed
+    replays only."""
     import torch
 
     import tensor_core_dense_gb300 as tcg
@@ -347,16 +349,33 @@ def time_graph(rot, steps, warmup, sampler=None):
     torch.cuda.synchronize()
     g.replay()  # one untimed replay
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
     if sampler is not None:
         sampler.start()
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize()
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(world)
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        _barrier(world)
+        times.append(e0.elapsed_time(e1))
     if sampler is not None:
         sampler.stop()
-    return e0.elapsed_time(e1), launches, g
+    return times, launches, g
+
+
+def isa_peak_tflops(sms, sm_mhz, fp8=False):
+    """Dense tensor-core rate the instruction set allows at a clock: 8,192
+    BF16 (16,384 FP8) FLOP per SM per clock x SMs x clock.  The per-SM figure
+    is the B200 datasheet's, inferred in "How Blackwell's Tensor Memory
+    Actually Works" (peak arithmetic); on GB300 ncu's tensor-pipe counter
+    gives the same rate (about 8,200 BF16 and 16,400 FP8 FLOP/clk/SM)."""
+    if not sms or not sm_mhz:
+        return None
+    return (16384.0 if fp8 else 8192.0) * sms * sm_mhz * 1e6 / 1e12
 
 
 SECONDARY = ("bf16_256", "fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64",
@@ -410,8 +429,8 @@ def quant_config(name, steps, warmup, hbm_peak):
     """One quantiser workload: algorithmic bytes (X read once, codes and scales
     written once) per call over the mean call time."""
     rot = QuantRotation(name)
-    ms, launches, g = time_graph(rot, steps, warmup)
-    ms /= steps
+    times, launches, g = time_graph(rot, steps, warmup, replays=3)
+    ms = statistics.median(times) / steps
     nbytes = rot.input_bytes + rot.output_bytes
     gbs = nbytes / (ms * 1e-3) / 1e9
     out = {"workload": name, "rows": rot.rows, "cols": rot.cols,
@@ -435,8 +454,8 @@ def secondary_configs(steps=50, warmup=5, names=SECONDARY):
             continue
         w = W.make(name)
         rot = Rotation(w)
-        ms, _, g = time_graph(rot, steps, warmup)
-        ms /= steps
+        times, _, g = time_graph(rot, steps, warmup, replays=3)
+        ms = statistics.median(times) / steps
         out_bytes = w.M * w.N * (2 if w.out == "bf16" else 4)
         nbytes = rot.input_bytes + out_bytes
         nbytes += (w.a_scale.nbytes if w.a_scale is not None else 0) + (
@@ -450,28 +469,68 @@ def secondary_configs(steps=50, warmup=5, names=SECONDARY):
     return out
 
 
-def cpu_baseline_sample(w, seconds=12.0):
-    """The oracle as it stands, on seeded 128 x 128 output tiles of the workload,
-    until about `seconds` of wall time; TFLOPS of FP64 reference work."""
-    import numpy as np
+# Workloads the CPU baseline times, with their share of its time budget.
+CPU_BASELINE = ("bf16_256", "bf16_4096", "fp8_4096", "bf16_mlp", "fp8_skinny_16",
+                "fp8_skinny_64", "fp8_skinny_128")
 
+
+def _oracle_tiles(w, tiles, cores):
+    """The oracle as it stands on output tiles of a workload (values unused)."""
     import oracle
-    cores = oracle.default_threads()
-    rng = np.random.default_rng(0)
+    in_type = oracle.IN_BF16 if w.kind == "bf16" else oracle.IN_E4M3
+    mode = {"bf16": oracle.SCALE_NONE, "fp8_tensor": oracle.SCALE_TENSOR,
+            "fp8_block": oracle.SCALE_BLOCK128}[w.kind]
+    c_type = oracle.C_BF16 if (w.C is not None and w.C.dtype.name == "uint16") else oracle.C_F32
+    return oracle.gemm(w.M, w.N, w.K, w.A, w.lda, w.B, w.ldb, in_type=in_type, scale_mode=mode,
+                       a_scale=w.a_scale, b_scale=w.b_scale, C=w.C,
+                       ldc=(w.C.shape[1] if w.C is not None else 0), c_type=c_type,
+                       alpha=w.alpha, beta=w.beta, tiles=tiles, nthreads=cores)
+
+
+def cpu_baseline_config(w, seconds, cores):
+    """Oracle wall time on a fixed tile set of one workload: the whole output
+    when it is small, else 128 x 128 tiles led by the first and the last tile
+    (then seeded ones, the parity tests' sampler), in batches of one tile per
+    core until about `seconds` have passed.  The full-output time is an
+    extrapolation from the sampled rate."""
+    import synth.workloads as W
+    if w.M * w.N <= 256 * 256:
+        tiles = [(0, 0, w.M, w.N)]
+    else:
+        tiles = W.sample_tiles(w.M, w.N, n=4096, size=128, seed=0)
     done_flops, t_used, ntiles = 0, 0.0, 0
-    batch = max(cores, 8)
-    while t_used < seconds:
-        tiles = [(int(rng.integers(0, w.M // 128)) * 128, int(rng.integers(0, w.N // 128)) * 128,
-                  128, 128) for _ in range(batch)]
+    while ntiles < len(tiles) and (ntiles == 0 or t_used < seconds):
+        batch = tiles[ntiles:ntiles + cores]
         t0 = time.perf_counter()
-        oracle.gemm(w.M, w.N, w.K, w.A, w.lda, w.B, w.ldb, tiles=tiles, nthreads=cores)
+        _oracle_tiles(w, batch, cores)
         t_used += time.perf_counter() - t0
-        done_flops += batch * 2 * 128 * 128 * w.K
-        ntiles += batch
-    return {"value": round(done_flops / t_used / 1e12, 6), "unit": "TFLOPS", "cores": cores,
+        done_flops += sum(2 * r * c * w.K for _, _, r, c in batch)
+        ntiles += len(batch)
+    rate = done_flops / t_used
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "tiles": ntiles,
+            "tile": "whole output" if len(tiles) == 1 else "128x128, first and last included",
+            "wall_s": round(t_used, 3), "gflops_fp64": round(rate / 1e9, 3),
+            "full_output_s_extrapolated": round(w.flops / rate, 1)}
+
+
+def cpu_baseline_sample(w_main, seconds=24.0):
+    """The oracle as it stands, timed on the host cores on every configured
+    workload (see cpu_baseline_config); `value` is its rate on the headline
+    workload in TFLOPS of FP64 reference work."""
+    import oracle
+    import synth.workloads as W
+    cores = oracle.default_threads()
+    per = []
+    for name in CPU_BASELINE:
+        w = w_main if name == w_main.name else W.make(name)
+        per.append(cpu_baseline_config(w, seconds / len(CPU_BASELINE), cores))
+    main = next(p for p in per if p["workload"] == w_main.name)
+    return {"value": round(main["gflops_fp64"] / 1e3, 6), "unit": "TFLOPS", "cores": cores,
             "kind": "oracle",
-            "sample": f"{ntiles} output tiles of 128x128 (K={w.K}) of the {w.M}x{w.N}x{w.K} "
-                      f"BF16 GEMM, FP64, {t_used:.1f} s"}
+            "sample": (f"{main['tiles']} output tiles of 128x128 (first and last included) of "
+                       f"the {w_main.M}x{w_main.N}x{w_main.K} BF16 GEMM, FP64, "
+                       f"{main['wall_s']:.1f} s; per_config lists every workload"),
+            "per_config": per}
 
 
 def run_ours(args):
@@ -497,19 +556,26 @@ def run_ours(args):
     except (OSError, AttributeError):
         nvml = None
         sampler = ClockSampler(smi_id)
-    # W warm-up steps, capture of the K timed steps, then the timed replay
-    # (barrier + synchronize on both sides inside time_graph's sync points)
+    # W warm-up steps, capture of the K timed steps, then R timed replays of
+    # them, each with a barrier and a synchronize on both sides; the median
+    # replay is the measurement
     _barrier(world)
-    total_ms, launches, graph = time_graph(rot, args.steps, args.warmup, nvml)
+    times, launches, graph = time_graph(rot, args.steps, args.warmup, nvml,
+                                        replays=args.replays, world=world)
     _barrier(world)
     clocks = ClockSampler.summary(nvml.rows if nvml is not None else sampler.stop())
-    clocks["source"] = "nvml, 1 ms, timed replay only" if nvml is not None else "nvidia-smi, 50 ms"
+    clocks["source"] = ("nvml, 1 ms, timed replays only" if nvml is not None
+                        else "nvidia-smi, 50 ms")
     assert tcg.last_device_status() == tcg.OK
     del graph
 
-    total_ms = _barrier_max(total_ms, world)
+    total_ms = _barrier_max(statistics.median(times), world)
     ms_per_step = total_ms / args.steps
     value = aggregate_tflops(w.flops, args.steps, total_ms, world)
+    replay_info = {"n": len(times), "statistic": "median",
+                   "ms": [round(t, 4) for t in times],
+                   "tflops_min": round(aggregate_tflops(w.flops, args.steps, max(times), world), 2),
+                   "tflops_max": round(aggregate_tflops(w.flops, args.steps, min(times), world), 2)}
 
     # end to end through the public API with host buffers: every step copies
     # its A and B in from pinned host memory, runs the GEMM and copies D out.
@@ -567,6 +633,9 @@ def run_ours(args):
 
     peak_bf16, _, peak_src = peaks()
     achieved = w.flops / (ms_per_step * 1e-3) / 1e12
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    isa = isa_peak_tflops(sms, clocks.get("sm_mhz"))
+    region_ms = sum(times)
     line = {
         "metric": "GEMM TFLOPS (BF16, FP8 E4M3) on 1 GB300; % of dense tensor-core peak",
         "value": round(value, 2),
@@ -584,17 +653,26 @@ def run_ours(args):
                                "BF16 output, alpha=1, beta=0",
                    "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{world}",
                    "l2": rot.describe(),
-                   "timing": "K back-to-back library calls captured in one CUDA graph, one "
-                             "CUDA-event pair around its replay"},
+                   "timing": f"K back-to-back library calls captured in one CUDA graph; "
+                             f"{args.replays} replays, each between a CUDA-event pair with a "
+                             f"barrier and a synchronize on both sides; value from the median "
+                             f"replay"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peak_bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_bf16, 4),
-                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "peak_source": f"{peak_src} bf16_tflops (burst: cuBLAS-class GEMM "
+                                    f"throughput measured on this pool)",
                      "frac_of_sustained": (round(achieved / sustained_peak(), 4)
-                                           if sustained_peak() else None),
+                                           if sustained_peak() and region_ms >= 100.0
+                                           else None),
+                     "isa_peak_at_clock": round(isa, 1) if isa else None,
+                     "frac_of_isa_peak_at_clock": round(achieved / isa, 4) if isa else None,
+                     "isa_peak_source": (f"8192 BF16 FLOP/clk/SM x {sms} SMs x the median SM "
+                                         f"clock sampled during the timed replays"),
                      "kernel": "gemm_tn2_kernel<bf16,bf16 out> (CTA pair)",
                      "traffic": stored_traffic() if args.traffic is None else args.traffic},
         "gpu_launches": launches,
+        "replays": replay_info,
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS",
                 "h2d_bytes_per_step": int(w.A.nbytes + w.B.nbytes),
@@ -610,10 +688,14 @@ def run_ours(args):
         for o in line["other_configs"]:
             if o["workload"] in QUANT:
                 continue
-            if o["workload"].startswith("fp8"):
+            fp8 = o["workload"].startswith("fp8")
+            if fp8:
                 o["frac_of_fp8_peak"] = round(o["tflops"] / (peak_bf16 * FP8_OVER_BF16), 4)
             else:
                 o["frac_of_bf16_peak"] = round(o["tflops"] / peak_bf16, 4)
+            isa_o = isa_peak_tflops(sms, clocks.get("sm_mhz"), fp8=fp8)
+            if isa_o:
+                o["frac_of_isa_peak_at_clock"] = round(o["tflops"] / isa_o, 4)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(w)
     if rank == 0:
@@ -683,6 +765,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--replays", type=int, default=5,
+                    help="timed replays of the K-step graph; the median is reported")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -19,18 +19,12 @@
  *
  * Every pointer is a device pointer owned by the caller.  A call enqueues
  * work on `stream` and returns without synchronising; D is valid once the
- * stream has reached that point.  The library allocates no memory per call:
- * it keeps a process-wide cache of TMA tensor maps (host memory) and, for the
- * split-K skinny path of the block-scaled FP8 GEMM, a per-device workspace
- * that is allocated on first use and grown when a larger one is needed.  A
- * call that would grow it while its stream is capturing a CUDA graph returns
- * TCG_ERR_UNSUPPORTED without enqueuing anything (make one call of that size
- * before capturing, or use gemm_fp8_e4m3_block_noalloc).  Calls on different
- * streams may run concurrently, except that block-scaled calls on the
- * split-K skinny kernel (M <= 128, and larger M where the pair tiles would
- * leave SMs idle) share that workspace and are serialised only by the stream
- * order the caller gives them; two such calls running concurrently on one
- * device race on it.  gemm_bf16 and per-tensor FP8 calls never use it.
+ * stream has reached that point.  No entry point allocates device memory:
+ * the library keeps a process-wide cache of TMA tensor maps (host memory),
+ * and gemm_fp8_e4m3_block_noalloc keeps a fixed scratch array in the
+ * library's device code (below).  Calls on different streams may run
+ * concurrently and are independent of one another, except calls of
+ * gemm_fp8_e4m3_block_noalloc, which share that array.
  *
  * No exception or abort crosses this boundary: every entry point returns a
  * tcg_status.  Argument errors are detected on the host before anything is
@@ -113,9 +107,13 @@ tcg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
  *                    swap-AB with A in one chunk; larger M runs on 256 x 256
  *                    CTA-pair tiles, or, when those would leave more than
  *                    half the SMs idle, in chunks of 128 rows of A (128 x 128
- *                    output tiles).  The result does not depend on the
- *                    choice beyond FP32 rounding order, and repeats bit for
- *                    bit for the same call.
+ *                    output tiles).  The swap-AB kernel splits each tile's K
+ *                    range over a cluster of two or three CTAs when the
+ *                    tiles fill at most half (a third) of the SMs, and
+ *                    otherwise gives each CTA whole tiles; no tile is ever
+ *                    finished through global memory.  The result does not
+ *                    depend on the choice beyond FP32 rounding order, and
+ *                    repeats bit for bit for the same call.
  */
 tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                          const void* B, int64_t ldb, const float* a_scale, const float* b_scale,
@@ -143,34 +141,46 @@ tcg_status gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                     float alpha, float beta, tcg_stream stream);
 
 /*
- * gemm_fp8_e4m3_block_noalloc -- the TCG_SCALE_BLOCK128 case of gemm_fp8_e4m3
- * without any device allocation.  The pages have no counterpart
- * to this entry point; it exists for callers that cannot let a library call
- * cudaMalloc: code being recorded into a CUDA graph (an allocation during
- * stream capture breaks the capture), latency-bound loops that cannot absorb
- * the device-wide synchronisation cudaMalloc/cudaFree can imply, and programs
- * whose own memory manager owns all of device memory.
+ * gemm_fp8_e4m3_block_noalloc -- the TCG_SCALE_BLOCK128 GEMM on the skinny
+ * kernel's stream-K form, whose scratch memory is a fixed array inside the
+ * library, so that nothing is allocated.  The pages have no counterpart to
+ * this entry point.
+ *
+ * Why it exists: past the sizes where a tile's K range splits over a
+ * cluster, gemm_fp8_e4m3 gives every CTA whole tiles, which leaves SMs idle
+ * when the tiles do not divide evenly over them (160 tiles on 152 SMs: 8
+ * CTAs take two).  The stream-K form cuts the K steps of all tiles into
+ * equal ranges and finishes tiles split between CTAs through global scratch
+ * (FP32 partial sums and per-tile counters).  A library that allocated that
+ * scratch itself would call cudaMalloc, which some callers cannot allow: a
+ * serving runtime or framework whose own allocator reserves all of device
+ * memory up front (an outside cudaMalloc fails, or fragments its pool), and
+ * latency-critical loops that cannot absorb the device-wide synchronisation
+ * cudaMalloc and cudaFree may imply.  Here the scratch is a file-scope
+ * __device__ array of 32 MiB, present on every device that loads the
+ * library until the process exits; the caller still provides A, B, the
+ * scales, C and D.
  *
  * Arguments, layouts, alignment and numerics are those of gemm_fp8_e4m3 with
- * mode = TCG_SCALE_BLOCK128.  M > 128 runs on the CTA-pair kernel, which
- * needs no scratch; so does M <= 128 when every N tile splits into two or
- * three pieces joined by a cluster (ceil(N/128) * 2 <= SMs).  Otherwise, for
- * M <= 128, the split-K scratch is a fixed 32 MiB array
- * inside the library's device code, present on every device that loads the
- * library until the process exits; the caller still provides A, B, the
- * scales, C and D.  A problem whose scratch would exceed 32 MiB (counters:
- * ceil(N/128) words rounded up to 256 bytes; partial sums: two Mp x 128 FP32
- * tiles per CTA of the launch, at most 152 CTAs x 64 KB; Mp = M rounded up to
- * 16/32/64/128) is rejected with TCG_ERR_UNSUPPORTED before anything is
- * enqueued.
+ * mode = TCG_SCALE_BLOCK128.  Kernel choice differs from gemm_fp8_e4m3 in
+ * two ways: M > 128 always runs the CTA-pair kernel (no scratch), even where
+ * gemm_fp8_e4m3 takes the 128-row chunks because few 256 x 256 tiles would
+ * leave SMs idle (such shapes may run slower here); M <= 128 runs the
+ * cluster-join form (no scratch) when ceil(N/128) * 2 <= SMs and K > 128,
+ * and the stream-K form otherwise.  A stream-K problem whose scratch would
+ * exceed 32 MiB is rejected with TCG_ERR_UNSUPPORTED before anything is
+ * enqueued: counters take ceil(N/128) 4-byte words rounded up to 256 bytes,
+ * partial sums two Mp x 128 FP32 tiles per CTA of the launch (Mp = M rounded
+ * up to 16/32/64/128; at most SMs x 128 KB).
  *
  * The first call on a device looks up the array's device address (with that
- * device current) and raises the kernel's shared-memory limit; make that
- * first call before any stream capture.  Each call with M <= 128 clears the
- * tile counters (a memset on `stream`) and then launches one kernel; M > 128
- * launches one kernel.  All calls on a device
- * share the one array: calls whose executions overlap on the GPU (different
- * streams without ordering between them) race on it and give wrong results.
+ * device current) and raises the kernels' shared-memory limits; make that
+ * first call before any stream capture.  A stream-K call clears the tile
+ * counters (a memset on `stream`), then launches one kernel; every other
+ * call launches one kernel.  All calls on a device share the one array and
+ * it keeps what the last call left: calls whose executions overlap on the
+ * GPU (different streams without ordering between them) race on it and give
+ * wrong results.
  */
 tcg_status gemm_fp8_e4m3_block_noalloc(int64_t M, int64_t N, int64_t K, const void* A,
                                        int64_t lda, const void* B, int64_t ldb,

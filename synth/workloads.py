@@ -117,3 +117,21 @@ def make(name: str, *, M=None, N=None, K=None) -> Workload:
         w.B, w.b_scale = e4m3_block128(values_f32(5, 2, N, K, out_prob=0.01, out_factor=50.0))
         return w
     raise KeyError(name)
+
+
+def sample_tiles(M, N, n=16, size=128, seed=0):
+    """Output tiles (i0, j0, rows, cols) for sampled checks and timings: the
+    first and the last tile plus seeded random ones, all clipped to the
+    matrix, first and last tile leading.  Tile selection only: no values."""
+    rng = np.random.default_rng(seed)
+    first, last = (0, 0), (max(0, M - size), max(0, N - size))
+    tiles = {first, last}
+    while len(tiles) < n:
+        i0 = int(rng.integers(0, max(1, M - size + 1)))
+        j0 = int(rng.integers(0, max(1, N - size + 1)))
+        tiles.add((i0, j0))
+        if len(tiles) >= max(1, M - size + 1) * max(1, N - size + 1):
+            break  # every position taken (tiny matrices)
+    order = [first] + ([last] if last != first else []) + sorted(tiles - {first, last})
+    return [(i0, j0, min(size, M - i0), min(size, N - j0)) for i0, j0 in order]
+

@@ -155,6 +155,14 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _beta(C, beta, what):
+    """beta as given; a non-zero beta needs a C to scale (the C call would
+    return ERR_INVALID_ARG for a NULL C)."""
+    if C is None and float(beta) != 0.0:
+        raise ValueError(f"{what}: beta = {beta} needs C")
+    return beta
+
+
 def gemm_bf16(A, B, D, C=None, *, alpha=1.0, beta=0.0, stream=None):
     """D = alpha * A @ B.T + beta * C on the GPU (BF16 A, B; D/C BF16 or FP32)."""
     import torch
@@ -168,7 +176,7 @@ def gemm_bf16(A, B, D, C=None, *, alpha=1.0, beta=0.0, stream=None):
         raise ValueError("C must match D")
     st = gemm_bf16_raw(M, N, K, _ptr(A), _ld(A, "A"), _ptr(B), _ld(B, "B"), _ptr(C),
                        _ld(C, "C") if C is not None else 0, _ptr(D), _ld(D, "D"), _out_dtype(D),
-                       alpha, beta if C is not None else 0.0, _stream_handle(stream))
+                       alpha, _beta(C, beta, "gemm_bf16"), _stream_handle(stream))
     if st != OK:
         raise TcgError(st, "gemm_bf16")
     return D
@@ -206,7 +214,7 @@ def gemm_fp8(A, B, a_scale, b_scale, D, C=None, *, mode=SCALE_TENSOR, a_format=N
         raise ValueError("C must match D")
     st = gemm_fp8_raw(M, N, K, _ptr(A), _ld(A, "A"), af, _ptr(B), _ld(B, "B"), bf, _ptr(a_scale),
                       _ptr(b_scale), mode, _ptr(C), _ld(C, "C") if C is not None else 0, _ptr(D),
-                      _ld(D, "D"), _out_dtype(D), alpha, beta if C is not None else 0.0,
+                      _ld(D, "D"), _out_dtype(D), alpha, _beta(C, beta, "gemm_fp8"),
                       _stream_handle(stream))
     if st != OK:
         raise TcgError(st, "gemm_fp8")
@@ -232,7 +240,7 @@ def gemm_fp8_e4m3(A, B, a_scale, b_scale, D, C=None, *, mode=SCALE_TENSOR, alpha
     st = gemm_fp8_e4m3_raw(M, N, K, _ptr(A), _ld(A, "A"), _ptr(B), _ld(B, "B"), _ptr(a_scale),
                            _ptr(b_scale), mode, _ptr(C), _ld(C, "C") if C is not None else 0,
                            _ptr(D), _ld(D, "D"), _out_dtype(D), alpha,
-                           beta if C is not None else 0.0, _stream_handle(stream))
+                           _beta(C, beta, "gemm_fp8_e4m3"), _stream_handle(stream))
     if st != OK:
         raise TcgError(st, "gemm_fp8_e4m3")
     return D

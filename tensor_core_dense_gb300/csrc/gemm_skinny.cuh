@@ -90,7 +90,10 @@ struct SkinnyParams {
   int32_t M, N, K;
   int32_t n_tiles, num_kb, total_steps, grid, max_seg;
   int32_t m_tiles;   // M in chunks of kMp rows (1 when M <= 128)
-  int32_t pad_m_;
+  // 1: CTA c takes whole tiles [c*tiles/grid, (c+1)*tiles/grid), all of K,
+  // so no tile is split and ws / counters are never touched; 0: the steps
+  // are cut into grid equal ranges (stream-K)
+  int32_t whole_tiles;
   const float* a_scale;  // [KB][M]
   const float* b_scale;  // [ceil(N/128)][KB]
   const void* C;
@@ -232,9 +235,11 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
   const int64_t T = p.total_steps, G = p.grid;
-  const int64_t s0 = sk_range_start(blockIdx.x, T, G);
-  const int64_t s1 = sk_range_start(blockIdx.x + 1, T, G);
   const int KB = p.num_kb;
+  const int64_t s0 = p.whole_tiles ? sk_range_start(blockIdx.x, T / KB, G) * KB
+                                   : sk_range_start(blockIdx.x, T, G);
+  const int64_t s1 = p.whole_tiles ? sk_range_start(blockIdx.x + 1, T / KB, G) * KB
+                                   : sk_range_start(blockIdx.x + 1, T, G);
   const int32_t m_tiles = kMChunks ? p.m_tiles : 1;
 
   if (threadIdx.x == 0) {

@@ -1,8 +1,10 @@
 // tcgemm.cu -- host side of the C ABI declared in include/tcgemm.h:
 // argument validation, TMA tensor-map encoding (cached), kernel selection and
 // launch.  The kernels themselves are in gemm_tn2.cuh / gemm_tn.cuh (BF16 and
-// per-tensor FP8) and gemm_skinny.cuh (block-scaled FP8, M <= 128); the FP8
-// quantiser's are in quant.cuh.
+// per-tensor FP8), gemm_skinny.cuh (decode-sized shapes and block-scaled FP8
+// in 128-row chunks) and gemm_tn2b.cuh (block-scaled FP8 on pair tiles); the
+// FP8 quantiser's are in quant.cuh.  No entry point allocates device memory;
+// gemm_fp8_e4m3_block_noalloc keeps a fixed scratch array in this module.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -181,56 +183,6 @@ tcg_status tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, const void* p
   if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
   g_maps.emplace(key, m);
   *out = m;
-  return TCG_OK;
-}
-
-// ---------------------------------------------------- skinny workspace
-
-struct Workspace {
-  void* ptr = nullptr;
-  size_t counter_cap = 0;  // bytes reserved for tile counters at the start
-  size_t partial_cap = 0;  // bytes of partial slots after them
-};
-Workspace g_ws[kMaxDevices];
-std::mutex g_ws_mu;
-
-// Per-device workspace: tile counters (one word per tile, kept zero between
-// calls) in a region of their own at the start, then the FP32 partial slots.
-// Both regions only grow; the partials always start after the whole counter
-// region, so no call's partial sums land on counter words a later call with
-// more tiles relies on being zero.
-tcg_status get_workspace(int dev, size_t counter_bytes, size_t partial_bytes, cudaStream_t stream,
-                         unsigned int** counters, float** partials) {
-  const size_t cbytes = (counter_bytes + 255) & ~size_t(255);
-  std::lock_guard<std::mutex> lk(g_ws_mu);
-  Workspace& w = g_ws[dev];
-  if (w.counter_cap < cbytes || w.partial_cap < partial_bytes) {
-    // Growing needs cudaDeviceSynchronize and cudaMalloc, which would break a
-    // CUDA graph being captured: refuse instead (the caller makes one call of
-    // the size before capturing, or uses the allocation-free entry point).
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return TCG_ERR_CUDA;
-    if (cs != cudaStreamCaptureStatusNone) return TCG_ERR_UNSUPPORTED;
-    const size_t ccap = w.counter_cap > cbytes ? w.counter_cap : cbytes;
-    const size_t pcap = w.partial_cap > partial_bytes ? w.partial_cap : partial_bytes;
-    if (w.ptr) {
-      if (cudaDeviceSynchronize() != cudaSuccess) return TCG_ERR_CUDA;
-      cudaFree(w.ptr);
-      w.ptr = nullptr;
-      w.counter_cap = w.partial_cap = 0;
-    }
-    void* p = nullptr;
-    if (cudaMalloc(&p, ccap + pcap) != cudaSuccess) return TCG_ERR_CUDA;
-    if (cudaMemsetAsync(p, 0, ccap, stream) != cudaSuccess) {  // counters start at zero
-      cudaFree(p);
-      return TCG_ERR_CUDA;
-    }
-    w.ptr = p;
-    w.counter_cap = ccap;
-    w.partial_cap = pcap;
-  }
-  *counters = static_cast<unsigned int*>(w.ptr);
-  *partials = reinterpret_cast<float*>(static_cast<char*>(w.ptr) + w.counter_cap);
   return TCG_OK;
 }
 
@@ -626,26 +578,16 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   const int64_t T = tiles * p.num_kb;
   if (T > INT32_MAX) return TCG_ERR_UNSUPPORTED;
   p.total_steps = (int32_t)T;
-  // With fewer N tiles than SMs, each tile's K range is cut into
-  // floor(SMs / tiles) equal pieces (at most 3), one per CTA, so a tile has
-  // few partial sums to add; otherwise the steps are spread over all SMs and
-  // every CTA gets at least ceil(KB/3) of them.  Either way at most kSkMaxSeg
-  // (4) CTAs share a tile.
-  int64_t split = 0;
-  {
-    int64_t g;
-    if (tiles < sms) {
-      split = sms / tiles;
-      if (split > 3) split = 3;
-      if (split > p.num_kb) split = p.num_kb;
-      g = tiles * split;
-    } else {
-      const int64_t min_steps = (p.num_kb + 2) / 3;
-      g = T / min_steps;
-      if (g > sms) g = sms;
-    }
-    p.grid = (int32_t)(g < 1 ? 1 : g);
-  }
+  // A tile's K range is cut into two or three pieces, one per CTA of a
+  // cluster that joins them in shared memory, when the tiles fill at most
+  // half (a third) of the SMs; otherwise every CTA takes whole tiles (grid =
+  // min(tiles, SMs), contiguous tile ranges) and writes D directly.  Neither
+  // form has a partial tile that crosses CTAs through global memory, so this
+  // entry point needs no workspace and calls on concurrent streams stay
+  // independent.
+  int64_t split = tiles < sms ? sms / tiles : 1;
+  if (split > 3) split = 3;
+  if (split > p.num_kb) split = p.num_kb;
   p.a_scale = sa;
   p.fp8_fmt = fp8_fmt_bits(a.b_fp8, a.a_fp8);  // swap-AB: UMMA A is B
   p.b_scale = sb;
@@ -657,30 +599,19 @@ tcg_status launch_skinny_inst(const Common& a, const float* sa, const float* sb,
   p.beta = a.beta;
   p.out_f32 = a.out == TCG_OUT_F32;
   p.has_c = a.beta != 0.0f;
-  if (split == 3 && !skinny_trio_fits<kMp, kIn, kScalar>(p.m_tiles > 1, tiles, dev)) {
+  if (split == 3 && !skinny_trio_fits<kMp, kIn, kScalar>(p.m_tiles > 1, tiles, dev))
     split = 2;  // fewer clusters of three fit at once than there are tiles
-    p.grid = (int32_t)(tiles * 2);
-  }
   if (split == 2 || split == 3) {
     // two or three pieces per tile: a cluster of their CTAs joins them in
     // shared memory (no workspace)
+    p.grid = (int32_t)(tiles * split);
     if (split == 2)
       return launch_skinny_join<kMp, 2, kIn, kScalar>(p.m_tiles > 1, ma, mb, p, stream, dev);
     return launch_skinny_join<kMp, 3, kIn, kScalar>(p.m_tiles > 1, ma, mb, p, stream, dev);
   }
-  // Segments per tile: a tile of num_kb steps meets at most
-  // ceil(num_kb / min_range) + 1 ranges, min_range = floor(T / grid).
-  const int64_t min_range = T / p.grid;
-  p.max_seg = (int32_t)((p.num_kb + min_range - 1) / min_range + 1);
-  if (p.max_seg > p.grid) p.max_seg = p.grid;
-  if (p.num_kb > 1) {  // a tile may be split over CTAs: needs the workspace
-    // two partial-tile slots per CTA (the first and the last piece of its range)
-    const size_t partial_bytes = (size_t)p.grid * 2 * kMp * 128 * sizeof(float);
-    if (tcg_status s = get_workspace(dev, (size_t)tiles * sizeof(unsigned int),
-                                     partial_bytes, stream, &p.counters, &p.ws);
-        s != TCG_OK)
-      return s;
-  }
+  p.whole_tiles = 1;
+  p.grid = (int32_t)(tiles < sms ? tiles : sms);
+  p.max_seg = 1;
   auto* fn = p.m_tiles > 1 ? &gemm_fp8_block_skinny_kernel<kMp, 0, kChunks, kIn, kScalar>
                            : &gemm_fp8_block_skinny_kernel<kMp, 0, false, kIn, kScalar>;
   if (tcg_status s = ensure_smem(fn, Cfg::kSmemBytes, dev); s != TCG_OK) return s;
@@ -860,12 +791,6 @@ tcg_status tcg_last_device_status(tcg_stream stream) {
   if (cudaMemcpyFromSymbol(&v, g_tcg_status, sizeof v) != cudaSuccess) return TCG_ERR_CUDA;
   if (v == 0) return TCG_OK;
   if (cudaMemcpyToSymbol(g_tcg_status, &zero, sizeof zero) != cudaSuccess) return TCG_ERR_CUDA;
-  // A timed-out split-K call may have left tile counters non-zero.
-  int dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
-    std::lock_guard<std::mutex> lk(g_ws_mu);
-    if (g_ws[dev].ptr) cudaMemset(g_ws[dev].ptr, 0, g_ws[dev].counter_cap);
-  }
   return TCG_ERR_TIMEOUT;
 }
 
@@ -918,17 +843,17 @@ tcg_status quantize_e4m3(int64_t rows, int64_t cols, const void* X, int64_t ldx,
 }  // extern "C"
 
 // ------------------------------------------------------------------------
-// Allocation-free variant of the block-scaled skinny FP8 path.
+// Allocation-free stream-K variant of the block-scaled skinny FP8 path.
 //
-// gemm_fp8_e4m3 allocates its split-K workspace with cudaMalloc on first use
-// (and again, after a device-wide synchronisation, whenever a larger one is
-// needed).  Some callers cannot allow that: code that records CUDA graphs
-// (an allocation inside stream capture invalidates the capture), serving
-// loops that must never stall on the implicit synchronisation of
-// cudaMalloc/cudaFree, and applications whose memory manager owns all of
-// device memory and forbids allocations behind its back.  For them,
-// gemm_fp8_e4m3_block_noalloc runs the same kernel with its scratch in a
-// fixed array that is part of the loaded module.
+// The regular entry points never need scratch: a tile's K range is split
+// only over the CTAs of one cluster, else each CTA takes whole tiles, which
+// leaves SMs idle when the tiles do not divide evenly over them.  The
+// stream-K form of the skinny kernel balances that by finishing tiles split
+// between any CTAs through global scratch.  Allocating it would mean calling
+// cudaMalloc, which some callers cannot allow: runtimes whose allocator owns
+// all of device memory, and latency-critical loops that cannot absorb the
+// device-wide synchronisation of cudaMalloc/cudaFree.  So this entry point
+// keeps the scratch in a fixed array that is part of the loaded module.
 namespace tcg {
 namespace {
 

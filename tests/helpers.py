@@ -145,11 +145,7 @@ def d_to_host(D):
 
 def sample_tiles(M, N, n=16, size=128, seed=0):
     """Output tiles for sampled parity: the first and last tiles plus seeded
-    random ones (all clipped to the matrix)."""
-    rng = np.random.default_rng(seed)
-    tiles = {(0, 0), (max(0, M - size), max(0, N - size))}
-    while len(tiles) < n:
-        i0 = int(rng.integers(0, max(1, M - size + 1)))
-        j0 = int(rng.integers(0, max(1, N - size + 1)))
-        tiles.add((i0, j0))
-    return [(i0, j0, min(size, M - i0), min(size, N - j0)) for i0, j0 in sorted(tiles)]
+    random ones (all clipped to the matrix); the same tiles bench.py's CPU
+    baseline times."""
+    from synth.workloads import sample_tiles as _tiles
+    return _tiles(M, N, n=n, size=size, seed=seed)

@@ -116,3 +116,20 @@ def test_quant_host_validation(tcg, args, want):
 def test_quant_fp8_format_validation(tcg):
     # an unknown FP8 format is refused before anything runs
     assert tcg.quantize_fp8_raw(8, 8, X, 8, 0, 7, 0, Q, 16, S, None) == 3
+
+
+def test_binding_refuses_beta_without_c():
+    # the tensor API must not turn a non-zero beta into 0 when C is missing:
+    # it raises before reaching the library (CPU tensors, nothing launched)
+    torch = pytest.importorskip("torch")
+    import tensor_core_dense_gb300 as t
+    A = torch.zeros((16, 16), dtype=torch.bfloat16)
+    D = torch.zeros((16, 16), dtype=torch.float32)
+    with pytest.raises(ValueError, match="needs C"):
+        t.gemm_bf16(A, A, D, None, beta=1.0)
+    A8 = torch.zeros((16, 16), dtype=torch.uint8)
+    s = torch.ones(1, dtype=torch.float32)
+    with pytest.raises(ValueError, match="needs C"):
+        t.gemm_fp8_e4m3(A8, A8, s, s, D, None, beta=-2.0)
+    with pytest.raises(ValueError, match="needs C"):
+        t.gemm_fp8(A8, A8, s, s, D, None, beta=0.5)

@@ -68,3 +68,24 @@ def test_nvml_sampler_fails_cleanly_without_a_device():
         pytest.skip("a GPU is present")
     with pytest.raises((OSError, AttributeError)):
         bench.NvmlSampler("GPU-00000000-0000-0000-0000-000000000000")
+
+
+def test_isa_peak_arithmetic():
+    # 8,192 BF16 FLOP/clk/SM x 152 SMs x 2.07 GHz; FP8 twice that
+    assert bench.isa_peak_tflops(152, 2070.0) == pytest.approx(2577.5, abs=0.1)
+    assert bench.isa_peak_tflops(152, 2070.0, fp8=True) == pytest.approx(5155.1, abs=0.1)
+    assert bench.isa_peak_tflops(152, None) is None
+
+
+def test_cpu_baseline_config_tiles_and_extrapolation():
+    import synth.workloads as W
+    w = W.make("bf16_256")
+    r = bench.cpu_baseline_config(w, 0.01, 2)
+    assert r["tiles"] == 1 and r["tile"] == "whole output"
+    assert r["full_output_s_extrapolated"] == pytest.approx(r["wall_s"], rel=0.05, abs=0.05)
+    w = W.make("fp8_skinny_16", N=8192, K=256)
+    r = bench.cpu_baseline_config(w, 0.0, 3)   # one batch: one tile per core
+    assert r["tiles"] == 3
+    # the fixed set leads with the first and the last tile
+    tiles = W.sample_tiles(16, 1024, n=8)
+    assert tiles[0][:2] == (0, 0) and tiles[1][:2] == (0, 1024 - 128)

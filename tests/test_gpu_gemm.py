@@ -138,8 +138,8 @@ def test_dense_kernels_both_paths(monkeypatch, kernel, M, N, K, kind, out, beta)
 
 # M <= 128 BF16 and per-tensor FP8 on the swap-AB skinny kernel (the library
 # routes decode-sized shapes there; TCG_KERNEL=skinny forces it): ragged M,
-# N and K, the cluster-pair split, the general split with the workspace,
-# beta*C, both output types.
+# N and K, the cluster-pair split, whole tiles per CTA (more N tiles than
+# half the SMs), beta*C, both output types.
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (7, 13, 50), (16, 1000, 1024), (33, 300, 2000),
                                    (64, 8192, 1024), (100, 2048, 3000), (128, 256, 64),
                                    (128, 20000, 512)])
@@ -297,9 +297,9 @@ def test_fp8_block_scaled_large_m(monkeypatch, kernel, M, N, K, out, beta):
     check_full(w, run(w))
 
 
-def test_fp8_block_workspace_reuse_across_shapes():
-    """A call with many tiles, one with few (whose partial sums must not land
-    on counter words), then the first shape again: all three correct."""
+def test_fp8_block_alternating_schedules():
+    """A call with many tiles (whole tiles per CTA), one with few (K split
+    over clusters), then the first shape again: all correct."""
     many = fp8_case(600, 4096, 1024, seed=91, mode="block", out="f32", outliers=0.01)
     few = fp8_case(16, 1000, 2048, seed=92, mode="block", out="f32", outliers=0.01)
     for w in (many, few, many, few):
@@ -581,42 +581,60 @@ def test_d_aliases_c_in_place(monkeypatch, case, out):
     check_full(w, D)
 
 
-def test_workspace_growth_refused_during_graph_capture(monkeypatch):
-    """A block-scaled call on the split-K skinny kernel whose workspace would
-    have to grow while its stream captures a CUDA graph is refused before
-    anything is enqueued (growing synchronises and allocates, which would
-    break the capture); the capture stays usable and the same call succeeds
-    outside it.  65,536 tiles (64 chunks of A x 1,024 N tiles) need more
-    tile counters than any other test."""
+def _block_case_device(w):
+    A, B = to_device(w.A)[:, :w.K], to_device(w.B)[:, :w.K]
+    return A, B, to_device(w.a_scale), to_device(w.b_scale)
+
+
+def test_block_scaled_concurrent_streams_independent():
+    """Block-scaled skinny calls past the cluster-join sizes (more N tiles
+    than SMs: whole tiles per CTA) on two streams with no ordering between
+    them, enqueued back to back so their kernels can overlap: each matches
+    the oracle.  The regular entry point keeps no state on the device, so
+    nothing is shared between the calls."""
     import tensor_core_dense_gb300 as tcg
-    monkeypatch.setenv("TCG_KERNEL", "skinny")
-    M, N, K = 8192, 131072, 256  # two K steps: tiles split over CTAs, partials in the workspace
-    A = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
-    B = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
-    sa = torch.ones(M * (K // 128), device="cuda")
-    sb = torch.ones((N // 128) * (K // 128), device="cuda")
-    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    probe = torch.zeros(4, device="cuda")
+    cases = [fp8_case(32, 20000, 1024, seed=71, mode="block", out="f32", outliers=0.01),
+             fp8_case(16, 28672, 2048, seed=72, mode="block", out="f32", outliers=0.01)]
+    dev = [_block_case_device(w) for w in cases]
+    Ds = [torch.full((w.M, w.N), float("nan"), device="cuda") for w in cases]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for w, (A, B, sa, sb), D, st in zip(cases, dev, Ds, streams):
+            tcg.gemm_fp8_e4m3(A, B, sa, sb, D, mode=tcg.SCALE_BLOCK128, stream=st)
+    torch.cuda.synchronize()
+    for w, D in zip(cases, Ds):
+        v, b = oracle_for(w)
+        check_f32("fp8", d_to_host(D), v, b, what=f"stream {w.M}x{w.N}x{w.K}")
+    assert tcg.last_device_status() == tcg.OK
+
+
+def test_block_scaled_whole_tiles_in_a_graph():
+    """The same whole-tile form captured in a CUDA graph and replayed twice:
+    the call does not allocate (an allocation would break the capture), the
+    replays leave the device's free memory unchanged, and each replay
+    matches the oracle."""
+    import tensor_core_dense_gb300 as tcg
+    w = fp8_case(32, 20000, 1024, seed=73, mode="block", out="bf16", outliers=0.01)
+    A, B, sa, sb = _block_case_device(w)
+    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    tcg.gemm_fp8_e4m3(A, B, sa, sb, D, mode=tcg.SCALE_BLOCK128)  # kernel loaded
+    torch.cuda.synchronize()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
-        probe.add_(1.0)
-        st = tcg.gemm_fp8_e4m3_raw(M, N, K, A.data_ptr(), K, B.data_ptr(), K, sa.data_ptr(),
-                                   sb.data_ptr(), tcg.SCALE_BLOCK128, None, 0, D.data_ptr(), N,
-                                   tcg.OUT_BF16, 1.0, 0.0, side.cuda_stream)
-    assert st == tcg.ERR_UNSUPPORTED
-    g.replay()
+        tcg.gemm_fp8_e4m3(A, B, sa, sb, D, mode=tcg.SCALE_BLOCK128, stream=side)
     torch.cuda.synchronize()
-    assert probe.tolist() == [1.0] * 4
-    st = tcg.gemm_fp8_e4m3_raw(M, N, K, A.data_ptr(), K, B.data_ptr(), K, sa.data_ptr(),
-                               sb.data_ptr(), tcg.SCALE_BLOCK128, None, 0, D.data_ptr(), N,
-                               tcg.OUT_BF16, 1.0, 0.0, torch.cuda.current_stream().cuda_stream)
-    assert st == tcg.OK
-    torch.cuda.synchronize()
-    assert (D[::1024, ::4096].float() == 0).all()
-    del D
-    torch.cuda.empty_cache()
+    free0 = torch.cuda.mem_get_info()[0]
+    v, b = oracle_for(w)
+    for _ in range(2):
+        D.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        check_bf16("fp8", d_to_host(D), v, b, what="graph replay")
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert tcg.last_device_status() == tcg.OK
 
 
 def test_fp8_block_pair_output_beyond_2_31_elements():
@@ -639,8 +657,8 @@ def test_fp8_block_pair_output_beyond_2_31_elements():
 
 
 def test_fp8_block_skinny_a_million_columns():
-    """N = 1,000,000 (7,813 N tiles, more than the SMs: the general stream-K
-    spread with the global workspace), ragged last tile."""
+    """N = 1,000,000 (7,813 N tiles, more than the SMs: contiguous ranges of
+    whole tiles per CTA), ragged last tile."""
     M, N, K = 16, 1_000_000, 256
     w = fp8_case(M, N, K, seed=62, mode="block", out="bf16", outliers=0.01)
     D = run(w)

@@ -1,5 +1,5 @@
 """The allocation-free block-scaled FP8 entry point, checked against the
-regular one.
+oracle.
 
 gemm_fp8_e4m3_block_noalloc is meant for callers that may not let a library
 allocate device memory: programs capturing CUDA graphs, latency-bound loops
@@ -12,11 +12,10 @@ also passes on its own in a fresh process.
 
 import ctypes
 
-import numpy as np
 import pytest
 
 import synth
-from helpers import TOL_FP8, d_to_host, oracle_for, to_device
+from helpers import c_values, check_bf16, check_f32, d_to_host, oracle_for, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -56,7 +55,7 @@ def _case(M, N, K, seed, out, beta):
                                             (32, 20000, 1024, "f32", 1.0),
                                             (300, 1000, 1024, "bf16", 1.0),
                                             (1024, 2048, 2048, "f32", 0.0)])
-def test_noalloc_matches_regular_entry_point_twice(M, N, K, out, beta):
+def test_noalloc_matches_oracle_twice(M, N, K, out, beta):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import tensor_core_dense_gb300 as tcg
@@ -69,10 +68,8 @@ def test_noalloc_matches_regular_entry_point_twice(M, N, K, out, beta):
     C = to_device(w.C) if w.C is not None else None
     if C is not None and C.dtype != dt:
         C = C.to(dt)
-    ref = torch.empty((M, N), dtype=dt, device="cuda")
-    tcg.gemm_fp8_e4m3(A, B, sa, sb, ref, C, mode=tcg.SCALE_BLOCK128, beta=beta)
-    want = d_to_host(ref)
-    _, bound = oracle_for(w)
+    v, bound = oracle_for(w)
+    c = c_values(w.C)
     stream = torch.cuda.current_stream().cuda_stream
     out_code = tcg.OUT_F32 if out == "f32" else tcg.OUT_BF16
     for call in range(2):  # the second call reuses the scratch the first one left
@@ -82,16 +79,11 @@ def test_noalloc_matches_regular_entry_point_twice(M, N, K, out, beta):
                 beta, stream)
         assert st == tcg.OK, tcg.status_string(st)
         got = d_to_host(D)
+        what = f"noalloc {M}x{N}x{K} {out} call {call}"
         if out == "bf16":
-            import oracle
-            g, r = oracle.bf16_decode(got), oracle.bf16_decode(want)
+            check_bf16("fp8", got, v, bound, beta, c, what=what)
         else:
-            g, r = got.astype(np.float64), want.astype(np.float64)
-        tol = 2 * TOL_FP8 * bound + 2.0 ** -22 * np.abs(r)
-        if out == "bf16":
-            tol = tol + 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -126))) - 7)
-        assert np.isfinite(g).all(), f"call {call}: non-finite output"
-        assert (np.abs(g - r) <= tol).all(), f"call {call}: differs from gemm_fp8_e4m3"
+            check_f32("fp8", got, v, bound, beta, c, what=what)
     assert tcg.last_device_status() == tcg.OK
 
 
