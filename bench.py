@@ -264,6 +264,10 @@ def make_call(w, A, B, D, C=None, sa=None, sb=None):
         def call():
             tcg.gemm_bf16(A, B, D, C, alpha=w.alpha, beta=w.beta,
                           stream=torch.cuda.current_stream())
+    elif w.kind == "fp8_mx":
+        def call():
+            tcg.gemm_mxfp8(A, B, sa, sb, D, C, a_format=w.a_fp8, b_format=w.b_fp8,
+                           alpha=w.alpha, beta=w.beta, stream=torch.cuda.current_stream())
     else:
         mode = tcg.SCALE_TENSOR if w.kind == "fp8_tensor" else tcg.SCALE_BLOCK128
 
@@ -309,8 +313,11 @@ class Rotation:
             C = None
             if w.C is not None:
                 C = torch.from_numpy(w.C.view(np.int16)).cuda().view(torch.bfloat16)
-            sa = torch.from_numpy(w.a_scale).cuda() if w.a_scale is not None else None
-            sb = torch.from_numpy(w.b_scale).cuda() if w.b_scale is not None else None
+            if w.kind == "fp8_mx":  # E8M0 scale bytes
+                sa, sb = torch.from_numpy(w.a_sf).cuda(), torch.from_numpy(w.b_sf).cuda()
+            else:
+                sa = torch.from_numpy(w.a_scale).cuda() if w.a_scale is not None else None
+                sb = torch.from_numpy(w.b_scale).cuda() if w.b_scale is not None else None
             self.tensors.append((A, B, C, D, sa, sb))
             self.calls.append(make_call(w, A, B, D, C, sa, sb))
 
@@ -379,7 +386,7 @@ def isa_peak_tflops(sms, sm_mhz, fp8=False):
 
 
 SECONDARY = ("bf16_256", "fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64",
-             "fp8_skinny_128", "fp8_block_4096", "bf16_skinny_16")
+             "fp8_skinny_128", "fp8_block_4096", "bf16_skinny_16", "mxfp8_4096")
 
 # The FP8 quantiser on the operands the FP8 workloads cast: (seed, tensor id,
 # rows, cols, granularity, outlier probability).  The values are the FP32
@@ -460,6 +467,8 @@ def secondary_configs(steps=50, warmup=5, names=SECONDARY):
         nbytes = rot.input_bytes + out_bytes
         nbytes += (w.a_scale.nbytes if w.a_scale is not None else 0) + (
             w.b_scale.nbytes if w.b_scale is not None else 0)
+        nbytes += (w.a_sf.nbytes if w.a_sf is not None else 0) + (
+            w.b_sf.nbytes if w.b_sf is not None else 0)
         out.append({"workload": name, "M": w.M, "N": w.N, "K": w.K,
                     "tflops": round(w.flops / (ms * 1e-3) / 1e12, 1),
                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 2),

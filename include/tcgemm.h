@@ -188,6 +188,38 @@ tcg_status gemm_fp8_e4m3_block_noalloc(int64_t M, int64_t N, int64_t K, const vo
                                        int64_t ldc, void* D, int64_t ldd, tcg_out_dtype out_dtype,
                                        float alpha, float beta, tcg_stream stream);
 
+/*
+ * gemm_mxfp8 -- D = alpha * sum over 32-wide K blocks kb of SFA[i,kb] *
+ * SFB[j,kb] * sum_{k in kb} A[i,k] B[k,j] + beta * C, with FP8 A and B (E4M3
+ * or E5M2 per operand, as gemm_fp8) and one E8M0 scale per row and 32-wide
+ * K block of each: the hardware block scaling of "How Blackwell's Tensor
+ * Memory Actually Works", section "Quantization became an allocation
+ * problem" (D = C + (A x SFA)(B x SFB), scale factors consumed by the tensor
+ * core; blocks of 32 with E8M0 scales, the microscaling format).  E8M0 code
+ * e is the scale 2^(e - 127).
+ *
+ * Layouts, C/D, alpha/beta, alignment and errors are those of gemm_fp8.
+ * a_sf, b_sf  device pointers to E8M0 bytes, 16-byte aligned, in tiles of
+ *             128 rows x 4 blocks (512 bytes): the scale of row r and block kb
+ *             is at byte ((r / 128) * KT + kb / 4) * 512 + (r % 32) * 16 +
+ *             ((r / 32) % 4) * 4 + kb % 4, KT = ceil(K / 128), for A with r =
+ *             i (ceil(M/128) * KT tiles) and for B with r = j (ceil(N/128) *
+ *             KT tiles).  Bytes of padding rows and blocks (r >= M or N, kb
+ *             >= ceil(K/32)) are read; those of padding blocks must not be
+ *             0xFF (NaN), which would reach real outputs through products
+ *             with the zero padding of A and B.
+ * Kernels     256 x 256 CTA-pair tiles; every product and scale is applied
+ *             by the tensor core, accumulation in FP32.  Nothing is
+ *             allocated; calls on different streams are independent.
+ * Errors      as gemm_fp8; NULL a_sf or b_sf: TCG_ERR_INVALID_ARG; a_sf or
+ *             b_sf not 16-byte aligned: TCG_ERR_ALIGNMENT.
+ */
+tcg_status gemm_mxfp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                      tcg_fp8_format a_format, const void* B, int64_t ldb,
+                      tcg_fp8_format b_format, const uint8_t* a_sf, const uint8_t* b_sf,
+                      const void* C, int64_t ldc, void* D, int64_t ldd, tcg_out_dtype out_dtype,
+                      float alpha, float beta, tcg_stream stream);
+
 /* Element type of the quantiser's input. */
 typedef enum { TCG_IN_F32 = 0, TCG_IN_BF16 = 1 } tcg_in_dtype;
 

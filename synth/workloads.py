@@ -17,7 +17,12 @@ Each workload is the synthetic stand-in for one of the pages' problems:
 * ``fp8_skinny_M`` FP8 E4M3 M in {16, 64, 128}, N = K = 8192, N(0, 1) with 1%
                   outliers x 50, 1 x 128 scales for A and 128 x 128 for B -- a
                   decode-sized batch ("How Blackwell's Tensor Memory Actually
-                  Works", "What this does to serving economics").
+                  Works", "What this does to serving economics");
+* ``mxfp8_4096``  microscaled FP8 4096^3: N(0, 1) with 1% outliers x 50, E4M3
+                  codes with one E8M0 scale per row and 32-wide K block of A
+                  and of B (the microscaling recipe), BF16 output -- the
+                  hardware block scaling of the same page, "Quantization
+                  became an allocation problem".
 
 Tensor ids: A = 1, B = 2, C = 3.  Seeds as listed below.
 """
@@ -28,7 +33,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import bf16, e4m3_block128, e4m3_rowblock, e4m3_tensor, values_f32
+from . import bf16, e4m3_block128, e4m3_rowblock, e4m3_tensor, mx_quant, mx_tile_sf, values_f32
 
 
 @dataclass
@@ -37,7 +42,7 @@ class Workload:
     M: int
     N: int
     K: int
-    kind: str            # "bf16" | "fp8_tensor" | "fp8_block"
+    kind: str            # "bf16" | "fp8_tensor" | "fp8_block" | "fp8_mx"
     out: str             # "bf16" | "f32"
     alpha: float = 1.0
     beta: float = 0.0
@@ -49,6 +54,8 @@ class Workload:
     meta: dict = field(default_factory=dict)
     a_fp8: int = 0        # FP8 encodings of A and B: 0 = E4M3, 1 = E5M2
     b_fp8: int = 0
+    a_sf: np.ndarray = None  # fp8_mx: E8M0 scale bytes of A and B, tiled layout
+    b_sf: np.ndarray = None
 
     @property
     def flops(self) -> int:
@@ -64,7 +71,7 @@ class Workload:
 
 
 NAMES = ("bf16_256", "bf16_4096", "fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64",
-         "fp8_skinny_128", "fp8_block_4096", "bf16_skinny_16")
+         "fp8_skinny_128", "fp8_block_4096", "bf16_skinny_16", "mxfp8_4096")
 
 
 def make(name: str, *, M=None, N=None, K=None) -> Workload:
@@ -108,6 +115,13 @@ def make(name: str, *, M=None, N=None, K=None) -> Workload:
         w = Workload(name, M, N, K, "fp8_block", "bf16")
         w.A, w.a_scale = e4m3_rowblock(values_f32(6, 1, M, K, out_prob=0.01, out_factor=50.0))
         w.B, w.b_scale = e4m3_block128(values_f32(6, 2, N, K, out_prob=0.01, out_factor=50.0))
+        return w
+    if name == "mxfp8_4096":
+        M, N, K = M or 4096, N or 4096, K or 4096
+        w = Workload(name, M, N, K, "fp8_mx", "bf16")
+        w.A, ea = mx_quant(values_f32(8, 1, M, K, out_prob=0.01, out_factor=50.0))
+        w.B, eb = mx_quant(values_f32(8, 2, N, K, out_prob=0.01, out_factor=50.0))
+        w.a_sf, w.b_sf = mx_tile_sf(ea, K), mx_tile_sf(eb, K)
         return w
     if name.startswith("fp8_skinny_"):
         M = M or int(name.rsplit("_", 1)[1])

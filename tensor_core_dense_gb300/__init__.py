@@ -8,7 +8,8 @@ missing, importing the binding's entry points raises.
     D = alpha * A @ B.T + beta * C      (A: M x K, B: N x K, both K-major)
 
 The entry points keep the C names: ``gemm_bf16``, ``gemm_fp8_e4m3``, ``gemm_fp8``
-(E4M3 / E5M2 per operand) and the FP8 quantiser ``quantize_e4m3`` that
+(E4M3 / E5M2 per operand), ``gemm_mxfp8`` (E8M0 scales per 32-wide K block,
+applied by the tensor core) and the FP8 quantiser ``quantize_e4m3`` that
 produces the FP8 GEMM's codes and scales.
 """
 
@@ -28,7 +29,7 @@ FP8_E4M3, FP8_E5M2 = 0, 1
 QUANT_TENSOR, QUANT_ROW128, QUANT_BLOCK128 = 0, 1, 2
 
 # Every symbol include/tcgemm.h declares.
-EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8", "gemm_fp8_e4m3_block_noalloc",
+EXPORTS = ("gemm_bf16", "gemm_fp8_e4m3", "gemm_fp8", "gemm_mxfp8", "gemm_fp8_e4m3_block_noalloc",
            "quantize_e4m3", "quantize_fp8", "tcg_status_string", "tcg_last_device_status", "tcg_launch_count",
            "tcg_debug_timeout_probe")
 
@@ -60,6 +61,9 @@ def lib():
         L.gemm_fp8.argtypes = [i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, vp, i32, vp, i64,
                                vp, i64, i32, f32, f32, vp]
         L.gemm_fp8.restype = i32
+        L.gemm_mxfp8.argtypes = [i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, vp, vp, i64,
+                                 vp, i64, i32, f32, f32, vp]
+        L.gemm_mxfp8.restype = i32
         L.quantize_e4m3.argtypes = [i64, i64, vp, i64, i32, i32, vp, i64, vp, vp]
         L.quantize_e4m3.restype = i32
         L.quantize_fp8.argtypes = [i64, i64, vp, i64, i32, i32, i32, vp, i64, vp, vp]
@@ -117,6 +121,12 @@ def gemm_fp8_raw(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale, b_scale, 
     return int(lib().gemm_fp8(M, N, K, A, lda, a_format, B, ldb, b_format, a_scale, b_scale,
                               mode, C, ldc, D, ldd, out_dtype, float(alpha), float(beta),
                               stream))
+
+
+def gemm_mxfp8_raw(M, N, K, A, lda, a_format, B, ldb, b_format, a_sf, b_sf, C, ldc, D, ldd,
+                   out_dtype, alpha, beta, stream) -> int:
+    return int(lib().gemm_mxfp8(M, N, K, A, lda, a_format, B, ldb, b_format, a_sf, b_sf, C,
+                                ldc, D, ldd, out_dtype, float(alpha), float(beta), stream))
 
 
 def quantize_e4m3_raw(rows, cols, X, ldx, x_dtype, mode, Q, ldq, scale, stream) -> int:
@@ -243,6 +253,40 @@ def gemm_fp8_e4m3(A, B, a_scale, b_scale, D, C=None, *, mode=SCALE_TENSOR, alpha
                            _beta(C, beta, "gemm_fp8_e4m3"), _stream_handle(stream))
     if st != OK:
         raise TcgError(st, "gemm_fp8_e4m3")
+    return D
+
+
+def mx_scale_bytes(rows, K):
+    """Bytes of one operand's E8M0 scales for gemm_mxfp8: ceil(rows/128) x
+    ceil(K/128) tiles of 512 bytes."""
+    return -(-rows // 128) * -(-K // 128) * 512
+
+
+def gemm_mxfp8(A, B, a_sf, b_sf, D, C=None, *, a_format=None, b_format=None, alpha=1.0,
+               beta=0.0, stream=None):
+    """D = alpha * sum_kb SFA * SFB * (A @ B.T over 32-wide K blocks) + beta * C
+    with FP8 A, B (float8_e4m3fn / float8_e5m2, or uint8 with a_format /
+    b_format) and E8M0 scale bytes a_sf, b_sf (uint8 or float8_e8m0fnu
+    tensors on the device, tiled layout in include/tcgemm.h)."""
+    import torch
+    af, bf = _fp8_format(A, a_format, "A"), _fp8_format(B, b_format, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    for t, n, rows in ((a_sf, "a_sf", M), (b_sf, "b_sf", N)):
+        if t.dtype not in (torch.uint8, getattr(torch, "float8_e8m0fnu", torch.uint8)):
+            raise ValueError(f"{n} must hold E8M0 bytes")
+        if not t.is_contiguous() or t.numel() < mx_scale_bytes(rows, K):
+            raise ValueError(f"{n} must be contiguous with mx_scale_bytes({rows}, K) bytes")
+    if C is not None and (tuple(C.shape) != (M, N) or C.dtype != D.dtype):
+        raise ValueError("C must match D")
+    st = gemm_mxfp8_raw(M, N, K, _ptr(A), _ld(A, "A"), af, _ptr(B), _ld(B, "B"), bf,
+                        _ptr(a_sf), _ptr(b_sf), _ptr(C), _ld(C, "C") if C is not None else 0,
+                        _ptr(D), _ld(D, "D"), _out_dtype(D), alpha,
+                        _beta(C, beta, "gemm_mxfp8"), _stream_handle(stream))
+    if st != OK:
+        raise TcgError(st, "gemm_mxfp8")
     return D
 
 

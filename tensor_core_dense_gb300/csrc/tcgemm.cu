@@ -16,6 +16,7 @@
 #include <unordered_map>
 #include <utility>
 
+#include "gemm_mx.cuh"
 #include "gemm_skinny.cuh"
 #include "gemm_tn.cuh"
 #include "gemm_tn2.cuh"
@@ -128,20 +129,25 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// A tensor map's identity; the planes fields are 0 for 2-D maps.
 struct MapKey {
   uint64_t ptr, inner, rows, ld_bytes;
   uint32_t dtype, box_inner, box_rows, swizzle;
+  uint64_t planes = 0, plane_bytes = 0;
+  uint32_t box_planes = 0;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && inner == o.inner && rows == o.rows && ld_bytes == o.ld_bytes &&
            dtype == o.dtype && box_inner == o.box_inner && box_rows == o.box_rows &&
-           swizzle == o.swizzle;
+           swizzle == o.swizzle && planes == o.planes && plane_bytes == o.plane_bytes &&
+           box_planes == o.box_planes;
   }
 };
 struct MapKeyHash {
   size_t operator()(const MapKey& k) const {
     uint64_t h = 1469598103934665603ull;
-    const uint64_t v[8] = {k.ptr,   k.inner,     k.rows,     k.ld_bytes,
-                           k.dtype, k.box_inner, k.box_rows, k.swizzle};
+    const uint64_t v[11] = {k.ptr,       k.inner,    k.rows,        k.ld_bytes,
+                            k.dtype,     k.box_inner, k.box_rows,   k.swizzle,
+                            k.planes,    k.plane_bytes, k.box_planes};
     for (uint64_t x : v) h = (h ^ x) * 1099511628211ull;
     return (size_t)h;
   }
@@ -178,6 +184,45 @@ tcg_status tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, const void* p
   const CUresult r = enc(&m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return TCG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+  g_maps.emplace(key, m);
+  *out = m;
+  return TCG_OK;
+}
+
+// A 3-D tensor (inner x rows x planes elements, row pitch ld_bytes, plane
+// pitch plane_bytes) read in boxes of box_inner x box_rows x box_planes,
+// without swizzling; out-of-range elements read as zero.
+tcg_status tensor_map_3d(CUtensorMap* out, CUtensorMapDataType dtype, const void* ptr,
+                         uint64_t inner, uint64_t rows, uint64_t planes, uint64_t ld_bytes,
+                         uint64_t plane_bytes, uint32_t box_inner, uint32_t box_rows,
+                         uint32_t box_planes) {
+  MapKey key{(uint64_t)(uintptr_t)ptr, inner,     rows,     ld_bytes,
+             (uint32_t)dtype,          box_inner, box_rows, (uint32_t)CU_TENSOR_MAP_SWIZZLE_NONE};
+  key.planes = planes;
+  key.plane_bytes = plane_bytes;
+  key.box_planes = box_planes;
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return TCG_OK;
+    }
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return TCG_ERR_CUDA;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof m);
+  const cuuint64_t dims[3] = {inner, rows, planes};
+  const cuuint64_t strides[2] = {ld_bytes, plane_bytes};
+  const cuuint32_t box[3] = {box_inner, box_rows, box_planes};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(&m, dtype, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return TCG_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_map_mu);
   if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
@@ -408,6 +453,65 @@ tcg_status launch_block_pair(const Common& a, const float* a_scale, const float*
 template <int kIn>
 tcg_status launch_skinny(const Common& a, const float* sa, const float* sb, bool scalar,
                          cudaStream_t stream);
+
+template <int kOut, bool kHasC>
+tcg_status launch_mx_inst(const CUtensorMap (&maps)[4], const MxParams& p, int grid, int dev,
+                          cudaStream_t stream) {
+  auto* fn = &gemm_mx_pair_kernel<kOut, kHasC>;
+  if (tcg_status s = ensure_smem(fn, kMxSmemBytes, dev); s != TCG_OK) return s;
+  if (launch_gemm_kernel(fn, grid, kMxThreads, kMxSmemBytes, stream, 2, maps[0], maps[1], maps[2],
+                         maps[3], p) != cudaSuccess)
+    return TCG_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
+}
+
+// Microscaled FP8 on 256 x 256 pair tiles (the schedule of launch_tn2): A
+// and B maps as the FP8 pair kernel's, and 3-D maps over the tiled E8M0
+// scales (128 four-byte words per 512-byte tile x K tiles x row tiles).
+tcg_status launch_mx(const Common& a, const uint8_t* a_sf, const uint8_t* b_sf,
+                     cudaStream_t stream) {
+  int dev, sms;
+  if (tcg_status s = current_device(&dev, &sms); s != TCG_OK) return s;
+  CUtensorMap maps[4];
+  Gemm2Params g;
+  int grid;
+  if (tcg_status s = pair_setup(a, 1, sms, &maps[0], &maps[1], &g, &grid); s != TCG_OK) return s;
+  const uint64_t kt = (uint64_t)((a.K + 127) / 128);
+  const uint64_t rta = (uint64_t)((a.M + 127) / 128), rtb = (uint64_t)((a.N + 127) / 128);
+  if (tcg_status s = tensor_map_3d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, a_sf, 128, kt, rta,
+                                   512, kt * 512, 128, 1, 1);
+      s != TCG_OK)
+    return s;
+  if (tcg_status s = tensor_map_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_UINT32, b_sf, 128, kt, rtb,
+                                   512, kt * 512, 128, 1, 2);
+      s != TCG_OK)
+    return s;
+  MxParams p{};
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.tiles_m = g.tiles_m;
+  p.tiles_n = g.tiles_n;
+  p.num_kb = g.num_kb;
+  p.num_tiles = g.num_tiles;
+  p.dp_waves = g.dp_waves;
+  p.dp_end = g.dp_end;
+  p.split = g.split;
+  p.fp8_fmt = g.fp8_fmt;
+  p.C = g.C;
+  p.ldc = g.ldc;
+  p.D = g.D;
+  p.ldd = g.ldd;
+  p.alpha = g.alpha;
+  p.beta = g.beta;
+  const bool has_c = a.beta != 0.0f;
+  if (a.out == TCG_OUT_BF16)
+    return has_c ? launch_mx_inst<0, true>(maps, p, grid, dev, stream)
+                 : launch_mx_inst<0, false>(maps, p, grid, dev, stream);
+  return has_c ? launch_mx_inst<1, true>(maps, p, grid, dev, stream)
+               : launch_mx_inst<1, false>(maps, p, grid, dev, stream);
+}
 
 // Decode-sized problems (M <= 128) are streams of B: the swap-AB skinny
 // kernel spreads them over the SMs in K, where the 128 x 256 tile kernel has
@@ -770,6 +874,26 @@ tcg_status gemm_fp8_e4m3(int64_t M, int64_t N, int64_t K, const void* A, int64_t
                          tcg_out_dtype out_dtype, float alpha, float beta, tcg_stream stream) {
   return gemm_fp8(M, N, K, A, lda, TCG_FP8_E4M3, B, ldb, TCG_FP8_E4M3, a_scale, b_scale, mode, C,
                   ldc, D, ldd, out_dtype, alpha, beta, stream);
+}
+
+tcg_status gemm_mxfp8(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                      tcg_fp8_format a_format, const void* B, int64_t ldb,
+                      tcg_fp8_format b_format, const uint8_t* a_sf, const uint8_t* b_sf,
+                      const void* C, int64_t ldc, void* D, int64_t ldd, tcg_out_dtype out_dtype,
+                      float alpha, float beta, tcg_stream stream) {
+  Common a{M, N, K, A, B, C, lda, ldb, ldc, ldd, D, (int)out_dtype, alpha, beta};
+  if ((a_format != TCG_FP8_E4M3 && a_format != TCG_FP8_E5M2) ||
+      (b_format != TCG_FP8_E4M3 && b_format != TCG_FP8_E5M2))
+    return TCG_ERR_UNSUPPORTED;
+  a.a_fp8 = (int)a_format;
+  a.b_fp8 = (int)b_format;
+  if (tcg_status s = validate(a, 1); s != TCG_OK) return s;
+  if (M == 0 || N == 0) return TCG_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return launch_k0(a, st);
+  if (!a_sf || !b_sf) return TCG_ERR_INVALID_ARG;
+  if (!aligned16(a_sf) || !aligned16(b_sf)) return TCG_ERR_ALIGNMENT;
+  return launch_mx(a, a_sf, b_sf, st);
 }
 
 const char* tcg_status_string(tcg_status status) {

@@ -67,14 +67,14 @@ def oracle_for(w, tiles=None, C_override=None, nthreads=None):
     """Oracle values and bounds for a synth.workloads.Workload."""
     in_type = oracle.IN_BF16 if w.kind == "bf16" else oracle.IN_E4M3
     mode = {"bf16": oracle.SCALE_NONE, "fp8_tensor": oracle.SCALE_TENSOR,
-            "fp8_block": oracle.SCALE_BLOCK128}[w.kind]
+            "fp8_block": oracle.SCALE_BLOCK128, "fp8_mx": oracle.SCALE_MX32}[w.kind]
     C = w.C if C_override is None else C_override
     c_type = oracle.C_BF16 if (C is not None and C.dtype == np.uint16) else oracle.C_F32
     return oracle.gemm(w.M, w.N, w.K, w.A, w.lda, w.B, w.ldb, in_type=in_type, scale_mode=mode,
                        a_scale=w.a_scale, b_scale=w.b_scale, C=C,
                        ldc=(C.shape[1] if C is not None else 0), c_type=c_type, alpha=w.alpha,
                        beta=w.beta, tiles=tiles, nthreads=nthreads, a_fp8=w.a_fp8,
-                       b_fp8=w.b_fp8)
+                       b_fp8=w.b_fp8, a_sf=w.a_sf, b_sf=w.b_sf)
 
 
 def c_values(C):
@@ -122,6 +122,10 @@ def run(w, out=None, C=None, alpha=None, beta=None, stream=None, D=None):
         D = torch.empty((w.M, -(-w.N // step) * step), dtype=dt, device="cuda")[:, :w.N]
     if w.kind == "bf16":
         tcg.gemm_bf16(A[:, :w.K], B[:, :w.K], D, Cd, alpha=alpha, beta=beta, stream=stream)
+    elif w.kind == "fp8_mx":
+        tcg.gemm_mxfp8(A[:, :w.K], B[:, :w.K], to_device(w.a_sf), to_device(w.b_sf), D, Cd,
+                       a_format=w.a_fp8, b_format=w.b_fp8, alpha=alpha, beta=beta,
+                       stream=stream)
     else:
         mode = tcg.SCALE_TENSOR if w.kind == "fp8_tensor" else tcg.SCALE_BLOCK128
         if w.a_fp8 == 0 and w.b_fp8 == 0:

@@ -133,3 +133,15 @@ def test_binding_refuses_beta_without_c():
         t.gemm_fp8_e4m3(A8, A8, s, s, D, None, beta=-2.0)
     with pytest.raises(ValueError, match="needs C"):
         t.gemm_fp8(A8, A8, s, s, D, None, beta=0.5)
+
+
+@pytest.mark.parametrize("args,want", [
+    ((8, 8, 16, A, 16, 0, B, 16, 0, None, B, None, 0, D, 8, 0, 1.0, 0.0), 1),   # no A scales
+    ((8, 8, 16, A, 16, 0, B, 16, 0, A, B + 8, None, 0, D, 8, 0, 1.0, 0.0), 2),  # B scales misaligned
+    ((8, 8, 16, A, 16, 2, B, 16, 0, A, B, None, 0, D, 8, 0, 1.0, 0.0), 3),      # bad A format
+    ((8, 8, 24, A, 24, 0, B, 32, 0, A, B, None, 0, D, 8, 0, 1.0, 0.0), 2),      # lda not x16
+    ((8, 8, 16, A, 16, 0, B, 16, 0, A, B, None, 0, D, 8, 0, 1.0, 1.0), 1),      # beta, no C
+    ((0, 8, 16, None, 0, 0, None, 0, 0, None, None, None, 0, None, 0, 0, 1.0, 0.0), 0),
+])
+def test_mxfp8_host_validation(tcg, args, want):
+    assert tcg.gemm_mxfp8_raw(*args, None) == want
