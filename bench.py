@@ -448,8 +448,10 @@ def quant_config(name, steps, warmup, hbm_peak):
     return out
 
 
-def secondary_configs(steps=50, warmup=5, names=SECONDARY):
-    """The other workloads, timed the same way (context beside the main line)."""
+def secondary_configs(steps=50, warmup=5, names=SECONDARY, size=None):
+    """The other workloads, timed the same way (context beside the main line);
+    size = (M, N, K) overrides a workload's shape (profiling a smaller case of
+    the same kernel)."""
     import torch
 
     import synth.workloads as W
@@ -459,7 +461,7 @@ def secondary_configs(steps=50, warmup=5, names=SECONDARY):
             out.append(quant_config(name, steps, warmup, peaks()[1]))
             torch.cuda.empty_cache()
             continue
-        w = W.make(name)
+        w = W.make(name) if size is None else W.make(name, M=size[0], N=size[1], K=size[2])
         rot = Rotation(w)
         times, _, g = time_graph(rot, steps, warmup, replays=3)
         ms = statistics.median(times) / steps
@@ -783,13 +785,16 @@ def main():
                     help="DRAM bytes per launch of the timed kernel from an ncu capture")
     ap.add_argument("--only", choices=SECONDARY + tuple(QUANT), default=None,
                     help="time one secondary workload alone (for profiling); prints its line")
+    ap.add_argument("--size", default=None,
+                    help="with --only: M,N,K overriding the workload's shape")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.only:
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        print(json.dumps(secondary_configs(args.steps, args.warmup, (args.only,))[0]))
+        size = tuple(int(x) for x in args.size.split(",")) if args.size else None
+        print(json.dumps(secondary_configs(args.steps, args.warmup, (args.only,), size)[0]))
         return
     if args.impl == "reference":
         run_reference(args)
