@@ -110,6 +110,41 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* map, 
       : "memory");
 }
 
+// 2-D tiled store of one box from this CTA's shared memory to global memory
+// (elements outside the tensor are not written), tracked as a bulk group of
+// the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+
+// Closes this thread's group of bulk copies issued since the last commit.
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until at most kN of this thread's bulk groups still read their
+// shared-memory source (the buffers of the others may be reused).
+template <int kN>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kN) : "memory");
+}
+
+// Waits until at most kN of this thread's bulk groups are incomplete.
+template <int kN>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(kN) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy accesses (a TMA store reading them).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Hint: bring one box of a tensor into L2 (no shared memory, no barrier).
 // L2 is coherent for the whole GPU, so this is safe before the grid
 // dependency wait even if the previous kernel is still writing the tensor.

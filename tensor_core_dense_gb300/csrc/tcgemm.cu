@@ -337,11 +337,13 @@ int forced_kernel() {
 }
 
 template <int kIn, int kOut, bool kHasC>
-tcg_status launch_tn2_inst(const CUtensorMap& ma, const CUtensorMap& mb, const Gemm2Params& p,
-                           int grid, int dev, cudaStream_t stream) {
+tcg_status launch_tn2_inst(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                           const CUtensorMap& mc, const Gemm2Params& p, int grid, int dev,
+                           cudaStream_t stream) {
   auto* fn = &gemm_tn2_kernel<kIn, kOut, kHasC>;
-  if (tcg_status s = ensure_smem(fn, kP2SmemBytes, dev); s != TCG_OK) return s;
-  if (launch_gemm_kernel(fn, grid, kThreads, kP2SmemBytes, stream, 2, ma, mb, p) != cudaSuccess)
+  if (tcg_status s = ensure_smem(fn, kP2DSmemBytes, dev); s != TCG_OK) return s;
+  if (launch_gemm_kernel(fn, grid, kThreads, kP2DSmemBytes, stream, 2, ma, mb, md, mc, p) !=
+      cudaSuccess)
     return TCG_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError() == cudaSuccess ? TCG_OK : TCG_ERR_CUDA;
@@ -415,11 +417,26 @@ tcg_status launch_tn2(const Common& a, const float* a_scale, const float* b_scal
   p.a_scale = a_scale;
   p.b_scale = b_scale;
   const bool has_c = a.beta != 0.0f;
-  if (a.out == TCG_OUT_BF16)
-    return has_c ? launch_tn2_inst<kIn, 0, true>(ma, mb, p, grid, dev, stream)
-                 : launch_tn2_inst<kIn, 0, false>(ma, mb, p, grid, dev, stream);
-  return has_c ? launch_tn2_inst<kIn, 1, true>(ma, mb, p, grid, dev, stream)
-               : launch_tn2_inst<kIn, 1, false>(ma, mb, p, grid, dev, stream);
+  // D (and C) as 2-D tensors for the epilogue's TMA stores (loads): boxes of
+  // 128 bytes (64 BF16 or 32 FP32 columns) x 32 rows, 128-byte swizzle
+  const bool bf16 = a.out == TCG_OUT_BF16;
+  const CUtensorMapDataType dto = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int osz = bf16 ? 2 : 4;
+  CUtensorMap md, mc;
+  if (tcg_status s = tensor_map(&md, dto, a.D, a.N, a.M, a.ldd * osz, 128 / osz, 32); s != TCG_OK)
+    return s;
+  mc = md;
+  if (has_c) {
+    if (tcg_status s = tensor_map(&mc, dto, a.C, a.N, a.M, a.ldc * osz, 128 / osz, 32);
+        s != TCG_OK)
+      return s;
+  }
+  if (bf16)
+    return has_c ? launch_tn2_inst<kIn, 0, true>(ma, mb, md, mc, p, grid, dev, stream)
+                 : launch_tn2_inst<kIn, 0, false>(ma, mb, md, mc, p, grid, dev, stream);
+  return has_c ? launch_tn2_inst<kIn, 1, true>(ma, mb, md, mc, p, grid, dev, stream)
+               : launch_tn2_inst<kIn, 1, false>(ma, mb, md, mc, p, grid, dev, stream);
 }
 
 template <int kOut, bool kHasC>
