@@ -16,12 +16,18 @@
 //   * each stage carries, beside A and B, this CTA's A scales (one 512-byte
 //     tile: 128 rows x 4 blocks) and the B scales of all 256 columns of the
 //     pair's tile (two such tiles: the tensor core of each SM reads the scales
-//     of every column from its own Tensor Memory), loaded by TMA through 3-D
-//     tensor maps (128 words x K tiles x row tiles) on the stage's mbarrier,
-//     tiles past the last row tile reading as zeros;
-//   * the MMA thread copies them to Tensor Memory (tcgen05.cp 32x128b.warpx4,
-//     issued before the stage's MMAs, which it orders), 12 columns per stage
-//     after the accumulator: A at +0, B at +4 and +8;
+//     of every column from its own Tensor Memory), loaded by TMA on the
+//     stage's mbarrier, tiles past the last row tile reading as zeros: A
+//     through a 3-D tensor map (128 words x K tiles x row tiles), B through a
+//     4-D one whose second dimension repeats each tile 4 times (stride 0), so
+//     the two B tiles land as the 128-row x 32-byte image, each lane quarter
+//     holding the 32-row pattern, that one copy spreads over 8 columns;
+//   * the MMA thread copies them to Tensor Memory, 12 columns per stage after
+//     the accumulator (A at +0 with tcgen05.cp 32x128b.warpx4, B at +4..+11
+//     with one 128x256b), issued before the stage's MMAs, which it orders.
+//     Each copy costs about 70 tensor cycles in the MMA stream whatever its
+//     size (three per stage measured 57.2 us at 4096^3, none 46.4), so the
+//     copies are as few and as large as the layout allows;
 //   * the accumulator takes 256 columns and the scale slots 72, so there is a
 //     single accumulator: eight epilogue warps read all of it into registers
 //     (128 columns each), hand it back, and only then scale, convert and
@@ -49,7 +55,7 @@ constexpr int kMxStages = 6;
 constexpr uint32_t kMxATileBytes = 128 * kBKBytes;     // this CTA's 128 rows of A
 constexpr uint32_t kMxBTileBytes = 128 * kBKBytes;     // its half of the B block
 constexpr uint32_t kMxSfaBytes = 512;                  // A scales of 128 rows x 4 blocks
-constexpr uint32_t kMxSfbBytes = 1024;                 // B scales of 256 rows x 4 blocks
+constexpr uint32_t kMxSfbBytes = 4096;  // B scales of 256 rows x 4 blocks, each tile 4 times
 constexpr uint32_t kMxStageBytes = kMxATileBytes + kMxBTileBytes;  // operand part (1024-aligned)
 constexpr int kMxThreads = 320;                        // producer, MMA, 8 epilogue warps
 constexpr int kMxNumBars = 2 * kMxStages + 3;          // full, empty, tfull, tempty, drain
@@ -87,6 +93,25 @@ __device__ __forceinline__ uint64_t smem_desc_sf_tile(uint32_t saddr) {
 __device__ __forceinline__ void tmem_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
+}
+
+// Shared-memory descriptor of the B-scale image as tcgen05.cp's 128x256b
+// shape reads it: 128 rows x 32 bytes, no swizzle, the rows' first 16 bytes
+// (the first tile, 4 times) in one 2 KB block and the second 16 bytes 2 KB
+// further (leading byte offset), 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sf_image(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(2048u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// Copies the 4 KB B-scale image into 8 Tensor Memory columns of all 128
+// lanes (each CTA of the pair from its own shared memory).
+__device__ __forceinline__ void tmem_cp_sf_image_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with E8M0 scales, both operands
@@ -217,7 +242,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             tma_load_2d_pair(b_smem(s) + (uint32_t)bx * kBBoxRows * kBKBytes, &tmap_b, fb,
                              kb * kBKBytes, brow0 + bx * kBBoxRows);
           tma_load_3d_pair(sfa_smem(s), &tmap_sfa, fb, 0, kb, arow0 / 128);
-          tma_load_3d_pair(sfb_smem(s), &tmap_sfb, fb, 0, kb, col0 / 128);
+          tma_load_4d_pair(sfb_smem(s), &tmap_sfb, fb, 0, 0, kb, col0 / 128);
         }
       }
       grid_launch_dependents();  // every load is issued: the next kernel may launch
@@ -266,8 +291,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t sfa_t = tmem_base + kMxSfColBase + s * kMxSfColsPerStage;
           const uint32_t sfb_t = sfa_t + 4u;
           tmem_cp_sf_pair(sfa_t, smem_desc_sf_tile(sfa_smem(s)));
-          tmem_cp_sf_pair(sfb_t, smem_desc_sf_tile(sfb_smem(s)));
-          if (nsub > 128) tmem_cp_sf_pair(sfb_t + 4u, smem_desc_sf_tile(sfb_smem(s) + 512u));
+          tmem_cp_sf_image_pair(sfb_t, smem_desc_sf_image(sfb_smem(s)));
           const uint64_t ad = smem_desc_k_sw128(a_smem(s));
           const uint64_t bd = smem_desc_k_sw128(b_smem(s));
 #pragma unroll

@@ -135,19 +135,22 @@ struct MapKey {
   uint32_t dtype, box_inner, box_rows, swizzle;
   uint64_t planes = 0, plane_bytes = 0;
   uint32_t box_planes = 0;
+  uint64_t cubes = 0, cube_bytes = 0;  // 4-D maps: fourth dimension
+  uint32_t box_cubes = 0;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && inner == o.inner && rows == o.rows && ld_bytes == o.ld_bytes &&
            dtype == o.dtype && box_inner == o.box_inner && box_rows == o.box_rows &&
            swizzle == o.swizzle && planes == o.planes && plane_bytes == o.plane_bytes &&
-           box_planes == o.box_planes;
+           box_planes == o.box_planes && cubes == o.cubes && cube_bytes == o.cube_bytes &&
+           box_cubes == o.box_cubes;
   }
 };
 struct MapKeyHash {
   size_t operator()(const MapKey& k) const {
     uint64_t h = 1469598103934665603ull;
-    const uint64_t v[11] = {k.ptr,       k.inner,    k.rows,        k.ld_bytes,
-                            k.dtype,     k.box_inner, k.box_rows,   k.swizzle,
-                            k.planes,    k.plane_bytes, k.box_planes};
+    const uint64_t v[14] = {k.ptr,       k.inner,       k.rows,       k.ld_bytes, k.dtype,
+                            k.box_inner, k.box_rows,    k.swizzle,    k.planes,   k.plane_bytes,
+                            k.box_planes, k.cubes,      k.cube_bytes, k.box_cubes};
     for (uint64_t x : v) h = (h ^ x) * 1099511628211ull;
     return (size_t)h;
   }
@@ -221,6 +224,47 @@ tcg_status tensor_map_3d(CUtensorMap* out, CUtensorMapDataType dtype, const void
   const cuuint32_t box[3] = {box_inner, box_rows, box_planes};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(&m, dtype, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return TCG_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+  g_maps.emplace(key, m);
+  *out = m;
+  return TCG_OK;
+}
+
+// A 4-D tensor (inner x rows x planes x cubes elements; pitches ld_bytes,
+// plane_bytes, cube_bytes, any of them may be 0 to repeat the data) read in
+// boxes without swizzling; out-of-range elements read as zero.
+tcg_status tensor_map_4d(CUtensorMap* out, CUtensorMapDataType dtype, const void* ptr,
+                         const uint64_t (&dims)[4], const uint64_t (&pitch)[3],
+                         const uint32_t (&box)[4]) {
+  MapKey key{(uint64_t)(uintptr_t)ptr, dims[0], dims[1], pitch[0],
+             (uint32_t)dtype,          box[0],  box[1],  (uint32_t)CU_TENSOR_MAP_SWIZZLE_NONE};
+  key.planes = dims[2];
+  key.plane_bytes = pitch[1];
+  key.box_planes = box[2];
+  key.cubes = dims[3];
+  key.cube_bytes = pitch[2];
+  key.box_cubes = box[3];
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return TCG_OK;
+    }
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return TCG_ERR_CUDA;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof m);
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {pitch[0], pitch[1], pitch[2]};
+  const cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(&m, dtype, 4, const_cast<void*>(ptr), d, st, b, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return TCG_ERR_CUDA;
@@ -500,8 +544,10 @@ tcg_status launch_mx(const Common& a, const uint8_t* a_sf, const uint8_t* b_sf,
                                    512, kt * 512, 128, 1, 1);
       s != TCG_OK)
     return s;
-  if (tcg_status s = tensor_map_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_UINT32, b_sf, 128, kt, rtb,
-                                   512, kt * 512, 128, 1, 2);
+  // B: each 512-byte tile read 4 times (a stride-0 dimension), two row tiles
+  // per box: the 128 x 32-byte image of one 128x256b Tensor Memory copy
+  if (tcg_status s = tensor_map_4d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_UINT32, b_sf,
+                                   {128, 4, kt, rtb}, {0, 512, kt * 512}, {128, 4, 1, 2});
       s != TCG_OK)
     return s;
   MxParams p{};
