@@ -134,6 +134,57 @@ __device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// One K step of the pair: the stage's A and B scales into Tensor Memory, the
+// four block-scaled MMAs of its 32-wide K blocks (block k: descriptors + 2k,
+// scale id k in the instruction descriptor and in bits 30-31 of both scale
+// addresses), and the commit of the stage to `done_bar` in both CTAs. As in
+// mma_step4_pair_test_next, the test of the next step's barrier is issued
+// first and its result read last, so that the issuing thread never waits on a
+// read-back with an empty tcgen05 queue; `idesc` is block 0's descriptor.
+__device__ __forceinline__ uint32_t mx_step_pair_test_next(
+    uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa_tmem,
+    uint32_t sfb_tmem, uint64_t sfa_sdesc, uint64_t sfb_sdesc, uint32_t accumulate,
+    uint32_t done_bar, uint32_t next_bar, uint32_t next_par) {
+  uint32_t ready;
+  asm volatile(
+      "{\n\t.reg .pred rdy, acc, one;\n\t"
+      ".reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      ".reg .b32 i1, i2, i3, sa1, sa2, sa3, sb1, sb2, sb3;\n\t"
+      "setp.ne.b32 acc, %9, 0;\n\t"
+      "setp.eq.b32 one, 0, 0;\n\t"
+      "add.s64 a1, %2, 2;\n\t"
+      "add.s64 a2, %2, 4;\n\t"
+      "add.s64 a3, %2, 6;\n\t"
+      "add.s64 b1, %3, 2;\n\t"
+      "add.s64 b2, %3, 4;\n\t"
+      "add.s64 b3, %3, 6;\n\t"
+      "or.b32 i1, %4, 0x20000010;\n\t"
+      "or.b32 i2, %4, 0x40000020;\n\t"
+      "or.b32 i3, %4, 0x60000030;\n\t"
+      "or.b32 sa1, %5, 0x40000000;\n\t"
+      "or.b32 sa2, %5, 0x80000000;\n\t"
+      "or.b32 sa3, %5, 0xC0000000;\n\t"
+      "or.b32 sb1, %6, 0x40000000;\n\t"
+      "or.b32 sb2, %6, 0x80000000;\n\t"
+      "or.b32 sb3, %6, 0xC0000000;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%11], %12;\n\t"
+      "tcgen05.cp.cta_group::2.32x128b.warpx4 [%5], %7;\n\t"
+      "tcgen05.cp.cta_group::2.128x256b [%6], %8;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %4, [%5], [%6], acc;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a1, b1, i1, [sa1], [sb1], one;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a2, b2, i2, [sa2], [sb2], one;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], a3, b3, i3, [sa3], [sb3], one;\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%10], %13;\n\t"
+      "selp.u32 %0, 1, 0, rdy;\n\t}"
+      : "=r"(ready)
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "l"(sfa_sdesc), "l"(sfb_sdesc), "r"(accumulate), "r"(done_bar), "r"(next_bar),
+        "r"(next_par), "h"((uint16_t)0x3)
+      : "memory");
+  return ready;
+}
+
 template <int kOut, bool kHasC>
 __global__ void __launch_bounds__(kMxThreads, 1)
     gemm_mx_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -278,9 +329,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t nsub = 256u / (uint32_t)w.split;
+        static_assert(kMmaPerStage == 4, "one K step is four 32-wide scale blocks");
+        const uint32_t idesc0 = make_idesc_mx(256, nsub, 0u) | p.fp8_fmt;
+        // The unit's first K step is waited for here; every later one was
+        // tested while the step before it was issued.
+        bool ready = false;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
-          if (!wait_phase(full_bar(s), ph, abort_flag, 0x43)) {
+          if (!ready && !wait_phase(full_bar(s), ph, abort_flag, 0x43)) {
             ok = false;
             break;
           }
@@ -290,19 +346,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           // producer could refill the stage
           const uint32_t sfa_t = tmem_base + kMxSfColBase + s * kMxSfColsPerStage;
           const uint32_t sfb_t = sfa_t + 4u;
-          tmem_cp_sf_pair(sfa_t, smem_desc_sf_tile(sfa_smem(s)));
-          tmem_cp_sf_image_pair(sfb_t, smem_desc_sf_image(sfb_smem(s)));
           const uint64_t ad = smem_desc_k_sw128(a_smem(s));
           const uint64_t bd = smem_desc_k_sw128(b_smem(s));
-#pragma unroll
-          for (int k = 0; k < kMmaPerStage; ++k) {
-            const uint32_t idesc = make_idesc_mx(256, nsub, (uint32_t)k) | p.fp8_fmt;
-            const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
-            mma_mx_pair(tmem_base, ad + 2u * k, bd + 2u * k, idesc,
-                        sfa_t | ((uint32_t)k << 30), sfb_t | ((uint32_t)k << 30), accumulate);
-          }
+          const bool more = kb + 1 < p.num_kb;
+          const uint32_t s1 = (it + 1u) % S, ph1 = ((it + 1u) / S) & 1u;
+          const uint32_t got = mx_step_pair_test_next(
+              tmem_base, ad, bd, idesc0, sfa_t, sfb_t, smem_desc_sf_tile(sfa_smem(s)),
+              smem_desc_sf_image(sfb_smem(s)), kb != 0 ? 1u : 0u, empty_bar(s),
+              more ? full_bar(s1) : full_bar(s), more ? ph1 : ph);
+          ready = more && got != 0u;
           issued = true;
-          tc_commit_pair(empty_bar(s), 0x3);
         }
         if (ok) tc_commit_pair(tfull_bar, 0x3);
       }

@@ -271,25 +271,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         const uint32_t idesc = (w.split == 1 ? kIdesc256 : kIdesc128) | (kIn == 1 ? p.fp8_fmt : 0u);
+        static_assert(kMmaPerStage == 4, "one K step is four 32-byte MMAs");
+        // The unit's first K step is waited for here; every later one was
+        // tested while the step before it was issued (see
+        // mma_step4_pair_test_next) and is waited for only if that test failed.
+        bool ready = false;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
-          if (!wait_phase(full_bar(s), ph, abort_flag, 0x23)) {
+          if (!ready && !wait_phase(full_bar(s), ph, abort_flag, 0x23)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint64_t ad = smem_desc_k_sw128(a_smem(s));
           const uint64_t bd = smem_desc_k_sw128(b_smem(s));
-#pragma unroll
-          for (int k = 0; k < kMmaPerStage; ++k) {
-            const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
-            if (kIn == 0)
-              mma_bf16_pair(d_tmem, ad + 2u * k, bd + 2u * k, idesc, accumulate);
-            else
-              mma_e4m3_pair(d_tmem, ad + 2u * k, bd + 2u * k, idesc, accumulate);
-          }
+          // test the next step of this unit; at the last step, a phase that is
+          // already complete (the result is not used)
+          const bool more = kb + 1 < p.num_kb;
+          const uint32_t s1 = (it + 1u) % S, ph1 = ((it + 1u) / S) & 1u;
+          const uint32_t got = mma_step4_pair_test_next<kIn>(
+              d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u, empty_bar(s), more ? full_bar(s1) : full_bar(s),
+              more ? ph1 : ph);
+          ready = more && got != 0u;
           issued = true;
-          tc_commit_pair(empty_bar(s), 0x3);
         }
         if (ok) tc_commit_pair(tfull_bar(acc), 0x3);
       }
