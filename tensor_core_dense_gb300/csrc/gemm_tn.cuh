@@ -384,25 +384,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         const uint32_t idesc = (w.split == 1 ? kIdesc256 : w.split == 2 ? kIdesc128 : kIdesc64) |
                                (kIn == 1 ? p.fp8_fmt : 0u);
+        static_assert(kMmaPerStage == 4, "one K step is four 32-byte MMAs");
+        // the unit's first K step is waited for here; every later one was
+        // tested while the step before it was issued (mma_step4_test_next)
+        bool ready = false;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-          if (!wait_phase(full_bar(s), ph, abort_flag, 3)) {
+          if (!ready && !wait_phase(full_bar(s), ph, abort_flag, 3)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint64_t ad = smem_desc_k_sw128(a_smem(s));
           const uint64_t bd = smem_desc_k_sw128(b_smem(s));
-#pragma unroll
-          for (int k = 0; k < kMmaPerStage; ++k) {
-            const uint32_t accumulate = (kb | k) != 0 ? 1u : 0u;
-            if (kIn == 0)
-              mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, idesc, accumulate);
-            else
-              mma_e4m3(d_tmem, ad + 2u * k, bd + 2u * k, idesc, accumulate);
-          }
+          const bool more = kb + 1 < p.num_kb;
+          const uint32_t s1 = (it + 1u) % kStages, ph1 = ((it + 1u) / kStages) & 1u;
+          const uint32_t got = mma_step4_test_next<kIn>(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u,
+                                                        empty_bar(s), more ? full_bar(s1) : full_bar(s),
+                                                        more ? ph1 : ph);
+          ready = more && got != 0u;
           issued = true;
-          tc_commit(empty_bar(s));
         }
         if (ok) tc_commit(tfull_bar(acc));
       }

@@ -527,8 +527,28 @@ __device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
-// One K step of a CTA pair: four MMAs D (+)= A * B^T over consecutive 32-byte
-// K slices (descriptors a_desc + 2k, b_desc + 2k), then a commit of this
+// Four MMAs D (+)= A * B^T over the consecutive 32-byte K slices of one
+// 128-byte K step: operand descriptors + 0, 2, 4, 6 (16-byte units), the
+// first slice accumulating into D when `acc`, the rest always. Expects the
+// predicates acc / one and the 64-bit registers a1..a3 / b1..b3 of
+// TCG_STEP4_SETUP; operands %1 (D), %2 (A), %3 (B), %4 (instruction desc.).
+// TCG_COMMIT_PAIR arrives on a barrier in both CTAs of the pair (mask: %8).
+#define TCG_STEP4_SETUP(ACC_OPERAND)                              \
+  ".reg .pred rdy, acc, one;\n\t"                                 \
+  ".reg .b64 a1, a2, a3, b1, b2, b3;\n\t"                         \
+  "setp.ne.b32 acc, " ACC_OPERAND ", 0;\n\t"                      \
+  "setp.eq.b32 one, 0, 0;\n\t"                                    \
+  "add.s64 a1, %2, 2;\n\tadd.s64 a2, %2, 4;\n\tadd.s64 a3, %2, 6;\n\t" \
+  "add.s64 b1, %3, 2;\n\tadd.s64 b2, %3, 4;\n\tadd.s64 b3, %3, 6;\n\t"
+#define TCG_STEP4_MMAS(GROUP, KIND)                                        \
+  "tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%1], %2, %3, %4, acc;\n\t" \
+  "tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%1], a1, b1, %4, one;\n\t" \
+  "tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%1], a2, b2, %4, one;\n\t" \
+  "tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%1], a3, b3, %4, one;\n\t"
+#define TCG_COMMIT_PAIR(BAR) \
+  "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [" BAR "], %8;\n\t"
+
+// One K step of a CTA pair: the four MMAs of the step, then a commit of the
 // step's operands to `done_bar` in both CTAs. Before the MMAs it tests
 // (without suspending) whether `next_bar` has completed the phase of parity
 // `next_par`, and returns that result at the end.
@@ -549,41 +569,57 @@ __device__ __forceinline__ uint32_t mma_step4_pair_test_next(uint32_t d_tmem, ui
                                                              uint32_t next_par) {
   uint32_t ready;
   if (kKind == 0) {
-    asm volatile(
-        "{\n\t.reg .pred rdy, acc, one;\n\t"
-        "setp.ne.b32 acc, %5, 0;\n\t"
-        "setp.eq.b32 one, 0, 0;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%7], %8;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %4, acc;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %9, %10, %4, one;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %11, %12, %4, one;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %13, %14, %4, one;\n\t"
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%6], %15;\n\t"
-        "selp.u32 %0, 1, 0, rdy;\n\t}"
-        : "=r"(ready)
-        : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(done_bar),
-          "r"(next_bar), "r"(next_par), "l"(a_desc + 2u), "l"(b_desc + 2u), "l"(a_desc + 4u),
-          "l"(b_desc + 4u), "l"(a_desc + 6u), "l"(b_desc + 6u), "h"((uint16_t)0x3)
-        : "memory");
+    asm volatile("{\n\t" TCG_STEP4_SETUP("%5")
+                 "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%6], %7;\n\t"
+                 TCG_STEP4_MMAS("2", "f16") TCG_COMMIT_PAIR("%9")
+                 "selp.u32 %0, 1, 0, rdy;\n\t}"
+                 : "=r"(ready)
+                 : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                   "r"(next_bar), "r"(next_par), "h"((uint16_t)0x3), "r"(done_bar)
+                 : "memory");
   } else {
-    asm volatile(
-        "{\n\t.reg .pred rdy, acc, one;\n\t"
-        "setp.ne.b32 acc, %5, 0;\n\t"
-        "setp.eq.b32 one, 0, 0;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%7], %8;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], %2, %3, %4, acc;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], %9, %10, %4, one;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], %11, %12, %4, one;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%1], %13, %14, %4, one;\n\t"
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%6], %15;\n\t"
-        "selp.u32 %0, 1, 0, rdy;\n\t}"
-        : "=r"(ready)
-        : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(done_bar),
-          "r"(next_bar), "r"(next_par), "l"(a_desc + 2u), "l"(b_desc + 2u), "l"(a_desc + 4u),
-          "l"(b_desc + 4u), "l"(a_desc + 6u), "l"(b_desc + 6u), "h"((uint16_t)0x3)
-        : "memory");
+    asm volatile("{\n\t" TCG_STEP4_SETUP("%5")
+                 "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%6], %7;\n\t"
+                 TCG_STEP4_MMAS("2", "f8f6f4") TCG_COMMIT_PAIR("%9")
+                 "selp.u32 %0, 1, 0, rdy;\n\t}"
+                 : "=r"(ready)
+                 : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                   "r"(next_bar), "r"(next_par), "h"((uint16_t)0x3), "r"(done_bar)
+                 : "memory");
+  }
+  return ready;
+}
+
+// One K step on one SM: four MMAs over the step's 32-byte K slices (the
+// first accumulating when `accumulate`), then a commit to `done_bar`, with a
+// test of `next_bar` (parity `next_par`) issued ahead of them and read after
+// -- the ordering of mma_step4_pair_test_next, for the same reason.
+template <int kKind>  // 0: kind::f16 (BF16), 1: kind::f8f6f4 (FP8)
+__device__ __forceinline__ uint32_t mma_step4_test_next(uint32_t d_tmem, uint64_t a_desc,
+                                                        uint64_t b_desc, uint32_t idesc,
+                                                        uint32_t accumulate, uint32_t done_bar,
+                                                        uint32_t next_bar, uint32_t next_par) {
+  uint32_t ready;
+  if (kKind == 0) {
+    asm volatile("{\n\t" TCG_STEP4_SETUP("%5")
+                 "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%6], %7;\n\t"
+                 TCG_STEP4_MMAS("1", "f16")
+                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+                 "selp.u32 %0, 1, 0, rdy;\n\t}"
+                 : "=r"(ready)
+                 : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                   "r"(next_bar), "r"(next_par), "r"(done_bar)
+                 : "memory");
+  } else {
+    asm volatile("{\n\t" TCG_STEP4_SETUP("%5")
+                 "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%6], %7;\n\t"
+                 TCG_STEP4_MMAS("1", "f8f6f4")
+                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+                 "selp.u32 %0, 1, 0, rdy;\n\t}"
+                 : "=r"(ready)
+                 : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                   "r"(next_bar), "r"(next_par), "r"(done_bar)
+                 : "memory");
   }
   return ready;
 }
