@@ -385,6 +385,22 @@ def isa_peak_tflops(sms, sm_mhz, fp8=False):
     return (16384.0 if fp8 else 8192.0) * sms * sm_mhz * 1e6 / 1e12
 
 
+def add_peak_fractions(o, peak_bf16, sms, sm_mhz):
+    """Adds to a GEMM workload's result `o` its fraction of the measured peak
+    of its input type (FP8 -- per-tensor, block-scaled or microscaled -- at
+    FP8_OVER_BF16 times the BF16 figure) and of the instruction-set rate at
+    the sampled clock."""
+    fp8 = "fp8" in o["workload"]
+    if fp8:
+        o["frac_of_fp8_peak"] = round(o["tflops"] / (peak_bf16 * FP8_OVER_BF16), 4)
+    else:
+        o["frac_of_bf16_peak"] = round(o["tflops"] / peak_bf16, 4)
+    isa_o = isa_peak_tflops(sms, sm_mhz, fp8=fp8)
+    if isa_o:
+        o["frac_of_isa_peak_at_clock"] = round(o["tflops"] / isa_o, 4)
+    return o
+
+
 SECONDARY = ("bf16_256", "fp8_4096", "bf16_mlp", "fp8_skinny_16", "fp8_skinny_64",
              "fp8_skinny_128", "fp8_block_4096", "bf16_skinny_16", "mxfp8_4096")
 
@@ -697,16 +713,8 @@ def run_ours(args):
     if rank == 0 and not args.no_secondary:
         line["other_configs"] = secondary_configs(names=SECONDARY + tuple(QUANT))
         for o in line["other_configs"]:
-            if o["workload"] in QUANT:
-                continue
-            fp8 = o["workload"].startswith("fp8")
-            if fp8:
-                o["frac_of_fp8_peak"] = round(o["tflops"] / (peak_bf16 * FP8_OVER_BF16), 4)
-            else:
-                o["frac_of_bf16_peak"] = round(o["tflops"] / peak_bf16, 4)
-            isa_o = isa_peak_tflops(sms, clocks.get("sm_mhz"), fp8=fp8)
-            if isa_o:
-                o["frac_of_isa_peak_at_clock"] = round(o["tflops"] / isa_o, 4)
+            if o["workload"] not in QUANT:
+                add_peak_fractions(o, peak_bf16, sms, clocks.get("sm_mhz"))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(w)
     if rank == 0:

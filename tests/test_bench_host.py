@@ -77,6 +77,21 @@ def test_isa_peak_arithmetic():
     assert bench.isa_peak_tflops(152, None) is None
 
 
+def test_peak_fractions_by_input_type():
+    """Every FP8 workload (per tensor, block-scaled, microscaled) is measured
+    against the FP8 rates, the BF16 ones against the BF16 rates."""
+    for name in ("fp8_4096", "fp8_block_4096", "fp8_skinny_128", "mxfp8_4096"):
+        o = bench.add_peak_fractions({"workload": name, "tflops": 2577.5}, 1000.0, 152, 2070.0)
+        assert "frac_of_bf16_peak" not in o
+        assert o["frac_of_fp8_peak"] == pytest.approx(2577.5 / (1000.0 * bench.FP8_OVER_BF16), abs=1e-4)
+        assert o["frac_of_isa_peak_at_clock"] == pytest.approx(0.5, abs=1e-4)
+    for name in ("bf16_4096", "bf16_mlp", "bf16_skinny_16"):
+        o = bench.add_peak_fractions({"workload": name, "tflops": 2577.5}, 1000.0, 152, 2070.0)
+        assert "frac_of_fp8_peak" not in o
+        assert o["frac_of_bf16_peak"] == pytest.approx(2.5775, abs=1e-4)
+        assert o["frac_of_isa_peak_at_clock"] == pytest.approx(1.0, abs=1e-4)
+
+
 def test_cpu_baseline_config_tiles_and_extrapolation():
     import synth.workloads as W
     w = W.make("bf16_256")
