@@ -316,6 +316,13 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
       uint32_t j = 0;
       uint32_t pc = 0;  // kAccTmem: pieces (a CTA's part of one tile) so far
       bool ok = true, issued = false;
+      // Each step's stage and (at a piece start) buffer were tested while the
+      // step before it was issued (mma_step4_test2_next) and are waited for
+      // only if a test failed. Not in the block-scaled Mp = 128 form: there the
+      // promotion warps bound the loop, and an MMA thread freed from its stalls
+      // only spins longer on their buffers, next to them (2 % slower).
+      constexpr bool kLookAhead = kScalar || kMp < 128;
+      bool rdy_full = false, rdy_free = false;
       for (int64_t st = s0; st < s1; ++st, ++j) {
         const uint32_t s = j % S, ph = (j / S) & 1u;
         const int kbs = (int)st - ((int)st / KB) * KB;
@@ -323,8 +330,8 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
         const bool piece_end = !kAccTmem || kbs == KB - 1 || st == s1 - 1;
         const uint32_t slot = kAccTmem ? pc : j;  // TMEM buffer sequence number
         const uint32_t b = slot % kSkNumAcc, bph = (slot / kSkNumAcc) & 1u;
-        if ((piece_start && !wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, 0x12)) ||
-            !wait_phase(full_bar(s), ph, abort_flag, 0x13)) {
+        if ((piece_start && !rdy_free && !wait_phase(tempty_bar(b), bph ^ 1u, abort_flag, 0x12)) ||
+            (!rdy_full && !wait_phase(full_bar(s), ph, abort_flag, 0x13))) {
           ok = false;
           break;
         }
@@ -332,20 +339,23 @@ __global__ void __launch_bounds__(SkinnyCfg<kMp>::kThreads, 1)
         const uint64_t ad = smem_desc_k_sw128(b_smem(s));  // UMMA A: 128 rows of B
         const uint64_t bd = smem_desc_k_sw128(a_smem(s));  // UMMA B: Mp rows of A
         const uint32_t d_tmem = tmem_base + b * kMp;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {  // 32 bytes of K per instruction
-          const uint32_t accumulate = (k != 0 || !piece_start) ? 1u : 0u;
-          if (kIn == 1)
-            mma_e4m3(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, accumulate);
-          else
-            mma_bf16(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, accumulate);
-        }
+        // The next step's stage and, if it starts a piece, its buffer. A test
+        // that is not needed reads this step's stage, whose phase cannot
+        // move before this step's own commit.
+        const bool more = kLookAhead && st + 1 < s1;
+        const bool next_start = !kAccTmem || (kbs + 1 == KB);
+        const uint32_t s_n = (j + 1u) % S, ph_n = ((j + 1u) / S) & 1u;
+        const uint32_t slot_n = kAccTmem ? pc + (piece_end ? 1u : 0u) : j + 1u;
+        const uint32_t b_n = slot_n % kSkNumAcc, bph_n = (slot_n / kSkNumAcc) & 1u;
+        const bool test_free = more && next_start;
+        const uint32_t got = mma_step4_test2_next<kIn>(
+            d_tmem, ad, bd, kIdesc, piece_start ? 0u : 1u, more ? full_bar(s_n) : full_bar(s),
+            more ? ph_n : ph, test_free ? tempty_bar(b_n) : full_bar(s), test_free ? bph_n ^ 1u : ph,
+            piece_end ? 1u : 0u, empty_bar(s), tfull_bar(b));
+        rdy_full = more && (got & 1u) != 0u;
+        rdy_free = test_free && (got & 2u) != 0u;
         issued = true;
-        tc_commit(empty_bar(s));
-        if (piece_end) {
-          tc_commit(tfull_bar(b));
-          ++pc;
-        }
+        if (piece_end) ++pc;
       }
       if (!ok && issued) {
         tc_commit(drain_bar);

@@ -590,6 +590,61 @@ __device__ __forceinline__ uint32_t mma_step4_pair_test_next(uint32_t d_tmem, ui
   return ready;
 }
 
+// A skinny-kernel K step on one SM: four MMAs over the step's 32-byte K
+// slices (the first accumulating when `accumulate`), a commit to `done_bar`
+// and, when `commit_full` is nonzero, one to `full_tmem_bar`. Ahead of them it
+// tests the next step's operand barrier (`next_bar`, parity `next_par`) and
+// Tensor Memory buffer barrier (`free_bar`, parity `free_par`); returns bit 0
+// / bit 1 for them -- the ordering of mma_step4_pair_test_next.
+template <int kKind>  // 0: kind::f16 (BF16), 1: kind::f8f6f4 (FP8)
+__device__ __forceinline__ uint32_t mma_step4_test2_next(uint32_t d_tmem, uint64_t a_desc,
+                                                         uint64_t b_desc, uint32_t idesc,
+                                                         uint32_t accumulate, uint32_t next_bar,
+                                                         uint32_t next_par, uint32_t free_bar,
+                                                         uint32_t free_par, uint32_t commit_full,
+                                                         uint32_t done_bar,
+                                                         uint32_t full_tmem_bar) {
+  uint32_t ready;
+  if (kKind == 0) {
+    asm volatile("{\n\t" TCG_STEP4_SETUP("%5")
+                 ".reg .pred fre, ctf;\n\t"
+                 ".reg .b32 fb;\n\t"
+                 "setp.ne.b32 ctf, %10, 0;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%6], %7;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 fre, [%8], %9;\n\t"
+                 TCG_STEP4_MMAS("1", "f16")
+                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t"
+                 "@ctf tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t"
+                 "selp.u32 fb, 2, 0, fre;\n\t"
+                 "selp.u32 %0, 1, 0, rdy;\n\t"
+                 "or.b32 %0, %0, fb;\n\t}"
+                 : "=r"(ready)
+                 : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                   "r"(next_bar), "r"(next_par), "r"(free_bar), "r"(free_par), "r"(commit_full),
+                   "r"(done_bar), "r"(full_tmem_bar)
+                 : "memory");
+  } else {
+    asm volatile("{\n\t" TCG_STEP4_SETUP("%5")
+                 ".reg .pred fre, ctf;\n\t"
+                 ".reg .b32 fb;\n\t"
+                 "setp.ne.b32 ctf, %10, 0;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 rdy, [%6], %7;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 fre, [%8], %9;\n\t"
+                 TCG_STEP4_MMAS("1", "f8f6f4")
+                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t"
+                 "@ctf tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t"
+                 "selp.u32 fb, 2, 0, fre;\n\t"
+                 "selp.u32 %0, 1, 0, rdy;\n\t"
+                 "or.b32 %0, %0, fb;\n\t}"
+                 : "=r"(ready)
+                 : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate),
+                   "r"(next_bar), "r"(next_par), "r"(free_bar), "r"(free_par), "r"(commit_full),
+                   "r"(done_bar), "r"(full_tmem_bar)
+                 : "memory");
+  }
+  return ready;
+}
+
 // One K step on one SM: four MMAs over the step's 32-byte K slices (the
 // first accumulating when `accumulate`), then a commit to `done_bar`, with a
 // test of `next_bar` (parity `next_par`) issued ahead of them and read after
