@@ -242,6 +242,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // the codes pass may start loading while the maxima pass drains: X is not
   // written by it (only scale[0] is, read after the dependency wait)
   if (kKind == kQuantAmax) grid_launch_dependents();
+  // Row and block quantisation are launched to overlap the previous kernel's
+  // tail (programmatic dependent launch): X, Q and the scales are touched
+  // only after it has finished.
+  if (kKind == kQuantRow || kKind == kQuantBlock) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+  }
 
   if (warp == kQConsumerWarps) {
     // ------------------------------------------------------------ producer

@@ -861,9 +861,9 @@ tcg_status launch_quant(int64_t rows, int64_t cols, const void* X, int64_t ldx,
   p.units = (int32_t)units;
   const int grid = (int)(units < sms ? units : sms);
   if (mode == TCG_QUANT_BLOCK128)
-    return launch_quant_inst<kIn, kQuantBlock, kFmt>(map, p, grid, dev, stream, false);
+    return launch_quant_inst<kIn, kQuantBlock, kFmt>(map, p, grid, dev, stream, true);
   if (mode == TCG_QUANT_ROW128)
-    return launch_quant_inst<kIn, kQuantRow, kFmt>(map, p, grid, dev, stream, false);
+    return launch_quant_inst<kIn, kQuantRow, kFmt>(map, p, grid, dev, stream, true);
   // per tensor: clear the running maximum, fold the per-CTA maxima, encode.
   // (Loading X with an evict-last policy in the first pass did not keep it in
   // L2 for the second on GB300; both passes read it from HBM.)
