@@ -126,27 +126,48 @@ class ClockSampler:
             if len(f) < 9:
                 continue
             try:
+                mask = int(f[4], 16)
+            except ValueError:
+                mask = 0
+            try:
                 rows.append(dict(sm=float(f[1]), max=float(f[2]),
                                  power=float(f[3]) if f[3] not in ("[N/A]", "") else 0.0,
-                                 hw=f[5], hw_thermal=f[6], sw_thermal=f[7], sw_power=f[8]))
+                                 hw=f[5], hw_thermal=f[6], sw_thermal=f[7], sw_power=f[8],
+                                 mask=mask))
             except ValueError:
                 continue
         return rows
 
+    # every clock-event reason bit the driver defines, for the raw masks
+    REASON_BITS = ((0x1, "gpu_idle"), (0x2, "applications_clocks_setting"),
+                   (0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x10, "sync_boost"),
+                   (0x20, "sw_thermal_slowdown"), (0x40, "hw_thermal_slowdown"),
+                   (0x80, "hw_power_brake_slowdown"), (0x100, "display_clock_setting"))
+
     @staticmethod
     def summary(rows):
+        """Median SM clock and the throttle reasons seen: `reasons` the four the
+        timing rules act on, `reasons_mask` the OR of every raw reason mask
+        sampled and `other_reasons` its remaining bits by name."""
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         reasons = set()
+        mask = 0
         for r in rows:
             for k, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
                             ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
                 if r[k].lower().startswith("active"):
                     reasons.add(name)
+            mask |= int(r.get("mask", 0))
+        other = sorted(name for bit, name in ClockSampler.REASON_BITS
+                       if mask & bit and name not in reasons and
+                       name not in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                    "sw_power_cap"))
         return {"sm_mhz": statistics.median(r["sm"] for r in rows),
                 "sm_max_mhz": max(r["max"] for r in rows),
                 "power_w_max": max(r["power"] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "reasons_mask": hex(mask),
+                "other_reasons": other, "samples": len(rows)}
 
 
 class NvmlSampler:
@@ -186,7 +207,8 @@ class NvmlSampler:
         act = lambda bit: "Active" if rs.value & bit else "Not Active"  # noqa: E731
         self.rows.append(dict(sm=float(c.value), max=self.max_mhz, power=pw.value / 1000.0,
                               hw=act(self.HW_SLOWDOWN), hw_thermal=act(self.HW_THERMAL),
-                              sw_thermal=act(self.SW_THERMAL), sw_power=act(self.SW_POWER_CAP)))
+                              sw_thermal=act(self.SW_THERMAL), sw_power=act(self.SW_POWER_CAP),
+                              mask=int(rs.value)))
 
     def _loop(self):
         while self.running:

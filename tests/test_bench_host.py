@@ -31,6 +31,21 @@ def test_clock_summary_median_and_reasons():
     assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
 
 
+def test_clock_summary_raw_reason_mask():
+    """The OR of the raw masks is kept, and bits outside the four the timing
+    rules act on are named (HW power brake, idle, ...)."""
+    rows = [_row(2070.0), _row(2070.0), _row(2070.0)]
+    rows[1]["mask"] = 0x80
+    rows[2]["mask"] = 0x1 | 0x4
+    rows[2]["sw_power"] = "Active"
+    s = bench.ClockSampler.summary(rows)
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["reasons_mask"] == "0x85"
+    assert s["other_reasons"] == ["gpu_idle", "hw_power_brake_slowdown"]
+    s = bench.ClockSampler.summary([_row(2070.0)])  # rows without a mask
+    assert s["reasons_mask"] == "0x0" and s["other_reasons"] == []
+
+
 def test_clock_summary_without_samples():
     s = bench.ClockSampler.summary([])
     assert s["samples"] == 0 and s["sm_mhz"] is None and s["reasons"] == []
