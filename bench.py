@@ -167,7 +167,10 @@ class ClockSampler:
                 "sm_max_mhz": max(r["max"] for r in rows),
                 "power_w_max": max(r["power"] for r in rows),
                 "reasons": sorted(reasons), "reasons_mask": hex(mask),
-                "other_reasons": other, "samples": len(rows)}
+                "other_reasons": other, "samples": len(rows),
+                **({"mem_mhz_min": min(r["mem"] for r in rows),
+                    "mem_mhz_max": max(r["mem"] for r in rows)}
+                   if all("mem" in r for r in rows) else {})}
 
 
 class NvmlSampler:
@@ -200,15 +203,16 @@ class NvmlSampler:
 
     def _sample(self):
         import ctypes
-        c, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        c, pw, rs, mc = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
         self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c))
+        self.lib.nvmlDeviceGetClockInfo(self.h, 2, ctypes.byref(mc))  # 2 = NVML_CLOCK_MEM
         self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
         self.reasons_fn(self.h, ctypes.byref(rs))
         act = lambda bit: "Active" if rs.value & bit else "Not Active"  # noqa: E731
         self.rows.append(dict(sm=float(c.value), max=self.max_mhz, power=pw.value / 1000.0,
                               hw=act(self.HW_SLOWDOWN), hw_thermal=act(self.HW_THERMAL),
                               sw_thermal=act(self.SW_THERMAL), sw_power=act(self.SW_POWER_CAP),
-                              mask=int(rs.value)))
+                              mask=int(rs.value), mem=float(mc.value)))
 
     def _loop(self):
         while self.running:

@@ -46,6 +46,14 @@ def test_clock_summary_raw_reason_mask():
     assert s["reasons_mask"] == "0x0" and s["other_reasons"] == []
 
 
+def test_clock_summary_memory_clock_range():
+    rows = [_row(2070.0), _row(2070.0)]
+    rows[0]["mem"], rows[1]["mem"] = 3996.0, 3200.0
+    s = bench.ClockSampler.summary(rows)
+    assert s["mem_mhz_min"] == 3200.0 and s["mem_mhz_max"] == 3996.0
+    assert "mem_mhz_min" not in bench.ClockSampler.summary([_row(2070.0)])
+
+
 def test_clock_summary_without_samples():
     s = bench.ClockSampler.summary([])
     assert s["samples"] == 0 and s["sm_mhz"] is None and s["reasons"] == []
