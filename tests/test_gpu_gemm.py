@@ -154,6 +154,42 @@ def test_dense_small_m_on_skinny_kernel(monkeypatch, M, N, K, kind, out, beta):
     check_full(w, run(w))
 
 
+# Units one or two K steps long (a step is 128 bytes of K) on many tiles per
+# CTA or pair: every step is also its unit's first or last, so the MMA
+# thread's test of the next step is skipped or falls on the next unit's first
+# stage, and tiles change every step or two.
+@pytest.mark.parametrize("kernel", ["1cta", "2cta"])
+@pytest.mark.parametrize("M,N,K,kind", [(4096, 2560, 64, "bf16"), (4096, 2560, 128, "bf16"),
+                                        (3000, 2600, 40, "bf16"), (4096, 2560, 128, "fp8"),
+                                        (4096, 2560, 256, "fp8"), (3000, 2600, 100, "fp8")])
+def test_one_and_two_step_units(monkeypatch, kernel, M, N, K, kind):
+    monkeypatch.setenv("TCG_KERNEL", kernel)
+    if kind == "bf16":
+        w = bf16_case(M, N, K, seed=M + N + K, out="f32")
+    else:
+        w = fp8_case(M, N, K, seed=M + N + K, mode="tensor", out="f32")
+    check_full(w, run(w))
+
+
+# The skinny kernel with K ranges of one or two steps per CTA: BF16 and
+# per-tensor FP8 (its one-scale form), and block-scaled FP8 at Mp = 64 (the
+# issue block) and Mp = 128 (the plain wait order).
+@pytest.mark.parametrize("M,K,kind", [(16, 64, "bf16"), (128, 128, "bf16"), (64, 128, "tensor"),
+                                      (128, 256, "tensor"), (64, 128, "block"),
+                                      (64, 256, "block"), (128, 128, "block"),
+                                      (128, 256, "block")])
+def test_skinny_one_and_two_step_ranges(monkeypatch, M, K, kind):
+    if kind == "bf16":
+        monkeypatch.setenv("TCG_KERNEL", "skinny")
+        w = bf16_case(M, 8192, K, seed=M + K, out="f32")
+    elif kind == "tensor":
+        monkeypatch.setenv("TCG_KERNEL", "skinny")
+        w = fp8_case(M, 8192, K, seed=M + K, mode="tensor", out="f32")
+    else:
+        w = fp8_case(M, 8192, K, seed=M + K, mode="block", out="f32", outliers=0.01)
+    check_full(w, run(w))
+
+
 def test_dense_small_m_skinny_deterministic(monkeypatch):
     monkeypatch.setenv("TCG_KERNEL", "skinny")
     w = bf16_case(64, 3000, 8192, seed=8, out="f32")

@@ -96,6 +96,15 @@ def test_mx_shapes(M, N, K, out, beta):
     check_full(w, run(w))
 
 
+# Units of one to three K steps (a step is 4 scale blocks, 128 K values) on
+# many tiles per pair: every step is also its unit's first or last.
+@pytest.mark.parametrize("M,N,K", [(4096, 2560, 32), (4096, 2560, 128), (4096, 2560, 256),
+                                   (3000, 2600, 352)])
+def test_mx_one_to_three_step_units(M, N, K):
+    w = mx_case(M, N, K, seed=M + N + K, out="f32")
+    check_full(w, run(w))
+
+
 @pytest.mark.parametrize("a_fmt,b_fmt", [(1, 1), (0, 1), (1, 0)])
 def test_mx_e5m2_operands(a_fmt, b_fmt):
     w = mx_case(384, 640, 768, seed=90 + 2 * a_fmt + b_fmt, a_fmt=a_fmt, b_fmt=b_fmt)
